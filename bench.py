@@ -1,9 +1,453 @@
-"""placeholder: metric formulas (full bench follows)."""
+"""Benchmark of the block-scaled FP8 hot path on GB300.
+
+Workload (one "step"): the dense block-FP8 GEMM shape sweep — m in
+{8, 64, 128, 1024, 2048, 4096} x (n, k) in {(4096, 7168), (7168, 18432),
+(18432, 7168), (24576, 1536), (32768, 512), (7168, 16384)} — where each of the
+36 shapes runs the per-token-group activation quant (1 x 128, fp32 scales)
+followed by the block-scaled GEMM against 128 x 128 block-quantized weights.
+Inputs are seeded synthetic tensors (activations N(0,1) with 0.1 % x50
+outliers, weights N(0, 0.02)), resident in HBM; the weights are quantized on
+the GPU before timing (offline, as on the pages).
+
+Metric: effective TFLOP/s of the whole step, sum(2 m n k) / step time, plus
+per-shape GEMM microseconds, TFLOP/s, GB/s (the pages' formula, "vLLM DeepGEMM
+FP8 Block GEMM 基准测试" §4.3) and fraction of the per-shape roofline.
+
+`--impl reference` times the CPU oracle (the only reference this method has)
+on a bounded sample of the same workload.  Under torchrun every rank runs the
+same workload on its own GPU (replicas, weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+SWEEP_NK = [(4096, 7168), (7168, 18432), (18432, 7168), (24576, 1536), (32768, 512),
+            (7168, 16384)]
+SWEEP_M = [8, 64, 128, 1024, 2048, 4096]
+METRIC = "block-FP8 GEMM TFLOPS & GB/s per (m,n,k); quant GB/s; % of roofline, 1 GB300"
+UNIT = "TFLOP/s"
+WORKLOAD = ("dense block-FP8 W8A8 shape sweep: m{8,64,128,1024,2048,4096} x "
+            "(n,k){(4096,7168),(7168,18432),(18432,7168),(24576,1536),(32768,512),"
+            "(7168,16384)}; per shape: 1x128 activation quant (fp32 scales) + 1x128/128x128 "
+            "block-scaled FP8 GEMM, fp32 accumulate, bf16 out")
+FP8_PER_BF16 = 2.0  # nominal dense fp8 : bf16 tensor-rate ratio on GB300 (4.5 : 2.25 PF)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# ---------------------------------------------------------------------------
+# the pages' metric formulas (§4.3)
+# ---------------------------------------------------------------------------
 def pages_tflops(m, n, k, t_us):
     return 2.0 * m * n * k / (t_us * 1e-6) / 1e12
 
 
 def pages_gbps(m, n, k, t_us):
     return (m * k + k * n + 2.0 * m * n) / (t_us * 1e-6) / 1e9
+
+
+def gemm_alg_bytes(m, n, k):
+    """Algorithmic bytes of one GEMM launch: fp8 A and W, bf16 out, fp32 scales."""
+    align4 = (m + 3) // 4 * 4
+    return m * k + n * k + 2 * m * n + align4 * (k // 128) * 4 + ((n + 127) // 128) * (k // 128) * 4
+
+
+def quant_alg_bytes(m, k):
+    """bf16 read + e4m3 write + fp32 column-major scales."""
+    return 2 * m * k + m * k + (m + 3) // 4 * 4 * (k // 128) * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("block_scaled_fp8_quant_gb300/csrc/gemm_kernels.cu",
+                "block_scaled_fp8_quant_gb300/csrc/bfq_device.cuh",
+                "block_scaled_fp8_quant_gb300/csrc/quant_kernels.cu"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic():
+    """DRAM bytes per step of the GEMM launches from the committed ncu summary,
+    or None when the summary is missing or was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "gemm_sweep_dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["gemm_dram_bytes_per_launch_avg"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+SAMPLE_ROWS = 8
+SAMPLE_COLS = 1024
+
+
+def oracle_sample_step():
+    """One bounded sample of the workload on the CPU oracle: 8 activation rows
+    against the first 2048 weight rows of each of the 6 (n, k) shapes (weight
+    block quant of that slice, activation quant, GEMM).  Returns FLOPs done."""
+    import numpy as np
+
+    import bfq_synth as synth
+    import oracle
+
+    flops = 0
+    for n, k in SWEEP_NK:
+        w = synth.weight(SAMPLE_COLS, k, seed=n + k)
+        x = synth.activation(SAMPLE_ROWS, k, seed=SAMPLE_ROWS * 31 + n)
+        wb = w.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
+        xb = x.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
+        wq, sw = oracle.weight_block_quant(wb, False)
+        aq, sa = oracle.quant(xb, oracle.FMT_F32)
+        oracle.gemm(aq, sa, oracle.FMT_F32, wq, sw)
+        flops += 2 * SAMPLE_ROWS * SAMPLE_COLS * k
+    return flops
+
+
+def cpu_baseline():
+    import oracle
+
+    oracle.build_oracle()
+    t0 = time.perf_counter()
+    flops = oracle_sample_step()
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{SAMPLE_ROWS} activation rows x first {SAMPLE_COLS} weight rows of "
+                      f"each of the 6 (n,k) sweep shapes: weight block quant + activation "
+                      f"quant + fp64 block GEMM, single thread ({dt:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+
+    oracle.build_oracle()
+    for _ in range(args.warmup):
+        oracle_sample_step()
+    t0 = time.perf_counter()
+    flops = 0
+    for _ in range(args.steps):
+        flops += oracle_sample_step()
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "bounded CPU sample"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{SAMPLE_ROWS} rows x {SAMPLE_COLS} weight rows per (n,k), "
+                                   f"per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def build_problem(bfq, torch, dev):
+    import bfq_synth as synth
+
+    shapes = []
+    for n, k in SWEEP_NK:
+        w = synth.weight(n, k, seed=n + k, device=dev)
+        wq, sw = bfq.weight_block_quant(w, bfq.SCALE_F32)
+        del w
+        for m in SWEEP_M:
+            x = synth.activation(m, k, seed=m * 31 + n, device=dev)
+            q = torch.empty((m, k), dtype=torch.float8_e4m3fn, device=dev)
+            s = torch.empty((k // 128, bfq.align4(m)), dtype=torch.float32, device=dev)
+            out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+            ws = bfq.gemm_workspace(m, n, k, dev)
+            shapes.append(dict(m=m, n=n, k=k, x=x, q=q, s=s, wq=wq, sw=sw, out=out, ws=ws))
+    torch.cuda.synchronize()
+    return shapes
+
+
+def step(bfq, shapes, events=None):
+    for i, sh in enumerate(shapes):
+        if events is not None:
+            events[i][0].record()
+        bfq.bfq_quant(sh["x"], sh["q"], sh["s"], bfq.SCALE_F32, sh["s"].shape[-1])
+        if events is not None:
+            events[i][1].record()
+        bfq.bfq_gemm_block_fp8(sh["q"], sh["s"], bfq.SCALE_F32, sh["s"].shape[-1], sh["wq"],
+                               sh["sw"], sh["out"], sh["ws"])
+        if events is not None:
+            events[i][2].record()
+
+
+def e2e_step(bfq, torch, shapes, host_x, host_out):
+    for sh, hx, ho in zip(shapes, host_x, host_out):
+        sh["x"].copy_(hx, non_blocking=True)
+        bfq.bfq_quant(sh["x"], sh["q"], sh["s"], bfq.SCALE_F32, sh["s"].shape[-1])
+        bfq.bfq_gemm_block_fp8(sh["q"], sh["s"], bfq.SCALE_F32, sh["s"].shape[-1], sh["wq"],
+                               sh["sw"], sh["out"], sh["ws"])
+        ho.copy_(sh["out"], non_blocking=True)
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import block_scaled_fp8_quant_gb300 as bfq
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    bfq.load_library()
+    peaks, peak_src = load_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    fp8_peak = float(peaks["bf16_tflops"]) * FP8_PER_BF16
+
+    shapes = build_problem(bfq, torch, dev)
+    n_shapes = len(shapes)
+    flops_step = sum(2 * s["m"] * s["n"] * s["k"] for s in shapes)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    for _ in range(args.warmup):
+        step(bfq, shapes)
+    torch.cuda.synchronize()
+
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_shapes)]
+              for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                      int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])) as clk:
+        start.record()
+        for i in range(args.steps):
+            step(bfq, shapes, events[i])
+        stop.record()
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = bfq.bfq_poll_device_status()
+    if status != 0:
+        raise RuntimeError(f"device watchdog reported status {status}")
+
+    # per-launch durations (median over the timed steps)
+    per_shape = []
+    gemm_ms_total = quant_ms_total = 0.0
+    for j, sh in enumerate(shapes):
+        qt = [events[i][j][0].elapsed_time(events[i][j][1]) for i in range(args.steps)]
+        gt = [events[i][j][1].elapsed_time(events[i][j][2]) for i in range(args.steps)]
+        gemm_ms_total += sum(gt)
+        quant_ms_total += sum(qt)
+        m, n, k = sh["m"], sh["n"], sh["k"]
+        g_us = statistics.median(gt) * 1e3
+        q_us = statistics.median(qt) * 1e3
+        t_roof = max(2.0 * m * n * k / (fp8_peak * 1e12), gemm_alg_bytes(m, n, k) / (hbm_peak * 1e9))
+        per_shape.append({
+            "m": m, "n": n, "k": k, "gemm_us": round(g_us, 2),
+            "tflops": round(pages_tflops(m, n, k, g_us), 1),
+            "gbps_pages": round(pages_gbps(m, n, k, g_us), 1),
+            "roofline_frac": round(t_roof * 1e6 / g_us, 3),
+            "bound": "tensor" if 2.0 * m * n * k / (fp8_peak * 1e12) >= gemm_alg_bytes(m, n, k) / (hbm_peak * 1e9) else "hbm",
+            "quant_us": round(q_us, 2),
+            "quant_gbps": round(quant_alg_bytes(m, k) / (q_us * 1e-6) / 1e9, 1),
+        })
+    gemm_launch_ms = gemm_ms_total / (args.steps * n_shapes)
+    achieved_tflops = flops_step * args.steps / (gemm_ms_total * 1e-3) / 1e12
+    gemm_bytes_avg = sum(gemm_alg_bytes(s["m"], s["n"], s["k"]) for s in shapes) / n_shapes
+    t_roof_sum = sum(max(2.0 * s["m"] * s["n"] * s["k"] / (fp8_peak * 1e12),
+                         gemm_alg_bytes(s["m"], s["n"], s["k"]) / (hbm_peak * 1e9)) for s in shapes)
+
+    # end to end through the public API with host buffers (pinned)
+    host_x = [s["x"].cpu().pin_memory() for s in shapes]
+    host_out = [torch.empty(s["out"].shape, dtype=torch.bfloat16).pin_memory() for s in shapes]
+    h2d = sum(x.numel() * 2 for x in host_x)
+    d2h = sum(o.numel() * 2 for o in host_out)
+    for _ in range(max(1, args.warmup)):
+        e2e_step(bfq, torch, shapes, host_x, host_out)
+    torch.cuda.synchronize()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record()
+    for _ in range(args.steps):
+        e2e_step(bfq, torch, shapes, host_x, host_out)
+    e_stop.record()
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_stop)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return 0
+    ms_per_step = total_ms / args.steps
+    traffic = profile_traffic()
+    line = {
+        "metric": METRIC,
+        "value": world * flops_step / (ms_per_step * 1e-3) / 1e12,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shapes": n_shapes, "act_scales": "fp32 col-major",
+                   "weight_scales": "fp32 128x128", "parallelism": f"replicas x{world}",
+                   "l2": "no flush: one step streams ~1.2 GB of distinct operands (> 129 MB "
+                         "L2) before any shape repeats"},
+        "e2e": {"value": world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * n_shapes * args.steps,
+        "roofline": {"bound": "tensor", "achieved": round(achieved_tflops, 1),
+                     "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": round(achieved_tflops / fp8_peak, 4),
+                     "traffic": traffic,
+                     "kernel": "gemm_block_fp8_kernel (all 36 sweep launches)",
+                     "peak_source": f"{peak_src} bf16 burst x {FP8_PER_BF16} (fp8:bf16 nominal)",
+                     "alg_bytes_per_launch_avg": gemm_bytes_avg,
+                     "avg_launch_us": round(gemm_launch_ms * 1e3, 2),
+                     "mixed_frac": round(t_roof_sum * 1e3 / (gemm_ms_total / args.steps), 4)},
+        "quant": {"total_us_per_step": round(quant_ms_total / args.steps * 1e3, 1),
+                  "hbm_peak_gbs": hbm_peak},
+        "clocks": clk.summary(),
+        "shapes": per_shape,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["bfq", "reference"], default="bfq")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        return run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

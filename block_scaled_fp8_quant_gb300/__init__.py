@@ -1,0 +1,256 @@
+"""block_scaled_fp8_quant_gb300 — block-scaled FP8 (W8A8) quant + GEMM for GB300.
+
+Thin Python binding over the C ABI of ``libbfq.so`` (declared in
+``include/bfq.h``).  Every step of the computation runs in the library's
+sm_103a CUDA kernels; this module only marshals torch tensors (device
+memory and the current stream) into the C calls.  There is no fallback: if
+the library cannot be built or loaded, or a call returns a non-zero status,
+a ``BfqError`` is raised.
+
+Functions named like the C entry points (``bfq_quant``, ``bfq_gemm_block_fp8``,
+...) take preallocated tensors; ``quant``, ``silu_mul_quant``,
+``weight_block_quant``, ``gemm`` and ``gemm_masked`` allocate their outputs
+with torch and call them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+SCALE_F32 = 0
+SCALE_F32_POW2 = 1
+SCALE_UE8M0_PACKED = 2
+
+STATUS_NAMES = {
+    0: "BFQ_OK", 1: "BFQ_ERR_INVALID_ARG", 2: "BFQ_ERR_UNSUPPORTED_SHAPE",
+    3: "BFQ_ERR_MISALIGNED", 4: "BFQ_ERR_FORMAT", 5: "BFQ_ERR_CUDA", 6: "BFQ_ERR_TIMEOUT",
+    7: "BFQ_ERR_WORKSPACE", 8: "BFQ_ERR_DEVICE",
+}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+class BfqError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)} ({status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libbfq.so")
+
+
+def load_library(build: bool = True):
+    """Load libbfq.so (building it in-tree first when stale); raise if impossible."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build:
+            from . import _build
+
+            _build.build()
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libbfq.so not found at {path}: build the CUDA library first")
+        lib = ctypes.CDLL(path)
+        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        sig = {
+            "bfq_version": (I32, []),
+            "bfq_status_string": (ctypes.c_char_p, [I32]),
+            "bfq_quant": (I32, [P, I64, I64, I64, I32, I32, P, P, I64, P]),
+            "bfq_silu_mul_quant": (I32, [P, I32, I32, I32, P, I32, P, P, I64, P]),
+            "bfq_weight_block_quant": (I32, [P, I64, I64, I64, I32, P, P, P]),
+            "bfq_gemm_workspace_bytes": (SZ, [I64, I64, I64]),
+            "bfq_gemm_block_fp8": (I32, [P, P, I32, I64, P, P, I64, I64, I64, P, P, SZ, P]),
+            "bfq_gemm_block_fp8_masked": (I32, [P, P, I32, I64, P, P, P, I32, I32, I64, I64,
+                                                I32, P, P, SZ, P]),
+            "bfq_poll_device_status": (I32, [P]),
+            "bfq_watchdog_selftest": (I32, [I32, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise BfqError(fn, status)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def align4(n: int) -> int:
+    return (n + 3) // 4 * 4
+
+
+def scale_cols(k: int, fmt: int) -> int:
+    g = k // 128
+    return (g + 3) // 4 if fmt == SCALE_UE8M0_PACKED else g
+
+
+def scale_dtype(fmt: int) -> torch.dtype:
+    return torch.int32 if fmt == SCALE_UE8M0_PACKED else torch.float32
+
+
+# ---------------------------------------------------------------------------
+# C-ABI mirrors (preallocated tensors)
+# ---------------------------------------------------------------------------
+def bfq_quant(x, q, scales, fmt: int, scale_ld: int, group: int = 128, stream=None) -> None:
+    lib = load_library()
+    M, K = x.shape
+    _check("bfq_quant", lib.bfq_quant(_ptr(x), M, K, x.stride(0), group, fmt, _ptr(q),
+                                      _ptr(scales), scale_ld, _stream(stream)))
+
+
+def bfq_silu_mul_quant(x, valid_counts, q, scales, fmt: int, scale_ld: int,
+                       stream=None) -> None:
+    lib = load_library()
+    E, T, two_i = x.shape
+    assert x.is_contiguous() and q.is_contiguous()
+    _check("bfq_silu_mul_quant",
+           lib.bfq_silu_mul_quant(_ptr(x), E, T, two_i // 2, _ptr(valid_counts), fmt, _ptr(q),
+                                  _ptr(scales), scale_ld, _stream(stream)))
+
+
+def bfq_weight_block_quant(w, wq, sw, fmt: int, stream=None) -> None:
+    lib = load_library()
+    batch = 1 if w.dim() == 2 else w.shape[0]
+    N, K = w.shape[-2:]
+    assert w.is_contiguous() and wq.is_contiguous() and sw.is_contiguous()
+    _check("bfq_weight_block_quant",
+           lib.bfq_weight_block_quant(_ptr(w), batch, N, K, fmt, _ptr(wq), _ptr(sw),
+                                      _stream(stream)))
+
+
+def bfq_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().bfq_gemm_workspace_bytes(M, N, K))
+
+
+def bfq_gemm_block_fp8(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w_scales, out,
+                       workspace=None, stream=None) -> None:
+    lib = load_library()
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("bfq_gemm_block_fp8",
+           lib.bfq_gemm_block_fp8(_ptr(a_q), _ptr(a_scales), a_fmt, a_scale_ld, _ptr(w_q),
+                                  _ptr(w_scales), M, N, K, _ptr(out), _ptr(workspace), ws_bytes,
+                                  _stream(stream)))
+
+
+def bfq_gemm_block_fp8_masked(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w_scales,
+                              valid_counts, out, expected_m: int = 0, workspace=None,
+                              stream=None) -> None:
+    lib = load_library()
+    E, T, K = a_q.shape
+    N = w_q.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("bfq_gemm_block_fp8_masked",
+           lib.bfq_gemm_block_fp8_masked(_ptr(a_q), _ptr(a_scales), a_fmt, a_scale_ld,
+                                         _ptr(w_q), _ptr(w_scales), _ptr(valid_counts), E, T, N,
+                                         K, expected_m, _ptr(out), _ptr(workspace), ws_bytes,
+                                         _stream(stream)))
+
+
+def bfq_poll_device_status(stream=None) -> int:
+    return int(load_library().bfq_poll_device_status(_stream(stream)))
+
+
+def bfq_watchdog_selftest(timeout_us: int, stream=None) -> None:
+    _check("bfq_watchdog_selftest",
+           load_library().bfq_watchdog_selftest(timeout_us, _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# allocating helpers
+# ---------------------------------------------------------------------------
+def quant(x: torch.Tensor, fmt: int = SCALE_F32, scale_ld: int | None = None, stream=None):
+    """bf16 [M, K] -> (e4m3 [M, K], column-major scales [cols, scale_ld])."""
+    M, K = x.shape
+    ld = align4(M) if scale_ld is None else scale_ld
+    q = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=x.device)
+    s = torch.empty((scale_cols(K, fmt), ld), dtype=scale_dtype(fmt), device=x.device)
+    bfq_quant(x, q, s, fmt, ld, stream=stream)
+    return q, s
+
+
+def silu_mul_quant(x: torch.Tensor, valid_counts: torch.Tensor, fmt: int = SCALE_UE8M0_PACKED,
+                   scale_ld: int | None = None, stream=None):
+    """bf16 [E, T, 2I] -> (e4m3 [E, T, I], scales [E, cols, scale_ld]); padded rows untouched."""
+    E, T, two_i = x.shape
+    I = two_i // 2
+    ld = align4(T) if scale_ld is None else scale_ld
+    q = torch.empty((E, T, I), dtype=torch.float8_e4m3fn, device=x.device)
+    s = torch.empty((E, scale_cols(I, fmt), ld), dtype=scale_dtype(fmt), device=x.device)
+    bfq_silu_mul_quant(x, valid_counts, q, s, fmt, ld, stream=stream)
+    return q, s
+
+
+def weight_block_quant(w: torch.Tensor, fmt: int = SCALE_F32, stream=None):
+    """bf16 [N, K] or [B, N, K] -> (e4m3 same shape, fp32 [.., ceil(N/128), K/128])."""
+    N, K = w.shape[-2:]
+    lead = tuple(w.shape[:-2])
+    wq = torch.empty(w.shape, dtype=torch.float8_e4m3fn, device=w.device)
+    sw = torch.empty(lead + ((N + 127) // 128, K // 128), dtype=torch.float32, device=w.device)
+    bfq_weight_block_quant(w, wq, sw, fmt, stream=stream)
+    return wq, sw
+
+
+_ws_cache: dict = {}
+
+
+def gemm_workspace(M: int, N: int, K: int, device) -> torch.Tensor | None:
+    """Zero-initialised workspace sized for (M, N, K) on `device` (cached, grows)."""
+    need = bfq_gemm_workspace_bytes(M, N, K)
+    if need == 0:
+        return None
+    key = torch.device(device)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def gemm(a_q, a_scales, a_fmt: int, w_q, w_scales, out=None, workspace=None, stream=None):
+    """out[M, N] (bf16) = block-scaled A * W^T."""
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a_q.device)
+    if workspace is None:
+        workspace = gemm_workspace(M, N, K, a_q.device)
+    bfq_gemm_block_fp8(a_q, a_scales, a_fmt, a_scales.shape[-1], w_q, w_scales, out,
+                       workspace, stream=stream)
+    return out
+
+
+def gemm_masked(a_q, a_scales, a_fmt: int, w_q, w_scales, valid_counts, out=None,
+                expected_m: int = 0, stream=None):
+    """out[E, T, N] (bf16); rows r >= valid_counts[e] are not written."""
+    E, T, K = a_q.shape
+    N = w_q.shape[1]
+    if out is None:
+        out = torch.empty((E, T, N), dtype=torch.bfloat16, device=a_q.device)
+    bfq_gemm_block_fp8_masked(a_q, a_scales, a_fmt, a_scales.shape[-1], w_q, w_scales,
+                              valid_counts, out, expected_m, stream=stream)
+    return out

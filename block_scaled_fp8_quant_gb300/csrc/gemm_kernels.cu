@@ -1,0 +1,533 @@
+// gemm_kernels.cu — block-scaled FP8 GEMM on sm_103a tensor cores.
+//
+//   out[m, n] = sum_b sA[m, b] * sW[n / 128, b] * sum_{k in block b} a[m, k] w[n, k]
+//
+// ("vLLM DeepGEMM FP8 Block GEMM 基准测试" §4.2: fp8_gemm_nt and the Triton
+// loop that multiplies each K-block product by a_s * b_s; "[Kernel]
+// Integrate batched/masked deepgemm kernel": the masked per-expert form.)
+//
+// Design (one CTA per output tile and K split, one CTA per SM):
+//   warp 0      TMA producer: per 128-deep K block, one 128 x 128 A tile and
+//               one BN x 128 W tile (128-byte swizzle) into a smem ring.
+//   warp 1      allocates TMEM; lane 0 issues 4 tcgen05.mma (K = 32 each,
+//               kind::f8f6f4, e4m3 x e4m3 -> fp32) per K block into one of two
+//               TMEM partial-sum buffers, then commits to the ring's "empty"
+//               barrier and to the buffer's "full" barrier.
+//   warps 2..   epilogue ("promotion"): per K block, read the fp32 partial of
+//               its 32 rows x 128 columns from TMEM, multiply by the scale
+//               product sA[m, b] * sW[nblk, b] and accumulate in registers.
+//               At the end convert to bf16 and store the row, or (split-K)
+//               store fp32 partials; the last CTA of a tile to finish sums the
+//               splits in split order (deterministic) and stores bf16.
+// Every wait is bounded: a wait that gives up latches BFQ_ERR_TIMEOUT in the
+// library's status word, every role drains and the CTA frees its TMEM and
+// exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "bfq_device.cuh"
+
+namespace bfq {
+
+constexpr int kBM = 128;  // rows of A per tile (UMMA M)
+constexpr int kBK = 128;  // K per stage = one scale block
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kEpiWarps = BN / 32;  // 128 columns per warp
+  static constexpr int kThreads = 64 + kEpiWarps * 32;
+  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kBBytes = BN * kBK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBarrierBytes = 256;
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kBarrierBytes + 1024;
+};
+
+struct GemmParams {
+  const void* sa;          // activation scales (format a_fmt), column-major
+  int64_t sa_ld;           // leading dimension of sa
+  int64_t sa_estride;      // elements of sa per expert (masked)
+  const float* sw;         // weight scales [nblk][KB]
+  int64_t sw_estride;      // floats of sw per expert (masked)
+  __nv_bfloat16* out;      // [rows][N]
+  int64_t out_estride;     // elements of out per expert (masked)
+  float* ws;               // split-K partials [splits][M][N]
+  int* counters;           // split-K tile counters [tiles], zero between calls
+  const int32_t* counts;   // masked: per-expert valid rows
+  int* status;             // device error latch
+  int M;                   // dense: rows of A; masked: rows per expert (T)
+  int N, K;
+  int m_tiles, n_tiles, splits;
+  int a_fmt;
+};
+
+__device__ __forceinline__ float act_scale(const GemmParams& p, const void* sa, int kb, int m) {
+  if (p.a_fmt == BFQ_SCALE_UE8M0_PACKED) {
+    const uint32_t w = __ldg((const uint32_t*)sa + (int64_t)(kb >> 2) * p.sa_ld + m);
+    const uint32_t b = (w >> (8 * (kb & 3))) & 0xFFu;
+    return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);  // 2^(b-127)
+  }
+  return __ldg((const float*)sa + (int64_t)kb * p.sa_ld + m);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int BN, bool MASKED>
+__global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
+    gemm_block_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
+  using C = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::kStages * C::kABytes;
+  uint64_t* full = (uint64_t*)(smem + (size_t)C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = (uint32_t*)(drain + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
+
+  // ---- tile decode: split fastest, then m tile, then n tile, then expert ----
+  const int split = blockIdx.x % p.splits;
+  const int tile = blockIdx.x / p.splits;
+  const int mt = tile % p.m_tiles;
+  const int rest = tile / p.m_tiles;
+  const int nt = rest % p.n_tiles;
+  const int e = MASKED ? rest / p.n_tiles : 0;
+  const int m0 = mt * kBM, n0 = nt * BN;
+  int m_limit = p.M;
+  if (MASKED) {
+    int c = __ldg(p.counts + e);
+    m_limit = c < 0 ? 0 : (c > p.M ? p.M : c);
+    if (m0 >= m_limit) return;  // whole tile is padding: no loads, no MMA
+  }
+  const int KB = p.K / kBK;
+  const int kb_begin = (int)((int64_t)split * KB / p.splits);
+  const int kb_end = (int)((int64_t)(split + 1) * KB / p.splits);
+  const int nk = kb_end - kb_begin;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], C::kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      const int a_row = (MASKED ? e * p.M : 0) + m0;
+      const int w_row = (MASKED ? e * p.N : 0) + n0;
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % C::kStages;
+        const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)C::kStageBytes);
+        const int kx = (kb_begin + i) * kBK;
+        tma_load_2d_nohint(sA + (size_t)s * C::kABytes, &tmA, &full[s], kx, a_row);
+        tma_load_2d_nohint(sB + (size_t)s * C::kBBytes, &tmW, &full[s], kx, w_row);
+        ++issued;
+      }
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA can exit
+        for (int j = issued - C::kStages < 0 ? 0 : issued - C::kStages; j < issued; ++j) {
+          volatile int no_abort = 0;
+          (void)mbar_wait(&full[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, &no_abort,
+                          p.status, kWaitTimeoutNs / 8);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------- MMA issuer -------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+      bool issued_any = false;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % C::kStages;
+        const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+        const int buf = i & 1;
+        const uint32_t tph = (uint32_t)(i >> 1) & 1u;
+        if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
+        tc_fence_after_sync();
+        if (!mbar_wait(&full[s], ph, abort_flag, p.status, kWaitTimeoutNs)) break;
+        tc_fence_after_sync();
+        const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + (size_t)s * C::kABytes));
+        const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + (size_t)s * C::kBBytes));
+        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 32; ++kk)
+          umma_e4m3(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                    kk > 0 ? 1u : 0u);
+        umma_commit(&empty[s]);
+        umma_commit(&tfull[buf]);
+        issued_any = true;
+      }
+      if (*abort_flag && issued_any) {
+        // wait for the MMAs already issued before TMEM is released
+        umma_commit(drain);
+        volatile int no_abort = 0;
+        (void)mbar_wait(drain, 0, &no_abort, p.status, kWaitTimeoutNs / 8);
+      }
+    }
+  } else {
+    // ------------------------- epilogue / promotion ---------------------------
+    const int ew = warp - 2;
+    const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
+    const int half = (BN == 256) ? (ew >> 2) : 0;
+    const int row_local = quarter * 32 + lane;
+    const int m = m0 + row_local;
+    const bool row_ok = m < m_limit;
+    const int col0 = n0 + half * 128;
+    const bool warp_active = (m0 + quarter * 32 < m_limit) && (col0 < p.N);
+    const int ncols = min(128, p.N - col0);  // multiple of 64 when positive
+    const int nblk = col0 / 128;
+    const float* sw = p.sw + (MASKED ? (int64_t)e * p.sw_estride : 0) + (int64_t)nblk * KB;
+    const void* sa = MASKED ? (const void*)((const char*)p.sa +
+                                            (int64_t)e * p.sa_estride * 4)
+                            : p.sa;
+
+    float acc[128];
+#pragma unroll
+    for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+
+    for (int i = 0; i < nk; ++i) {
+      const int buf = i & 1;
+      const uint32_t tph = (uint32_t)(i >> 1) & 1u;
+      const int kb = kb_begin + i;
+      float sc = 0.0f;
+      if (warp_active) sc = (row_ok ? act_scale(p, sa, kb, m) : 0.0f) * __ldg(sw + kb);
+      if (!mbar_wait(&tfull[buf], tph, abort_flag, p.status, kWaitTimeoutNs)) break;
+      tc_fence_after_sync();
+      if (warp_active) {
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                               (uint32_t)(buf * BN + half * 128);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32_wait(taddr + (uint32_t)(c * 32), v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = __fmaf_rn(v[j], sc, acc[c * 32 + j]);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+
+    const bool ok = !*abort_flag;
+    const int64_t out_row = (MASKED ? (int64_t)e * p.out_estride : 0) + (int64_t)m * p.N;
+    if (p.splits == 1) {
+      if (ok && warp_active && row_ok) {
+        __nv_bfloat16* dst = p.out + out_row + col0;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (c * 8 < ncols)
+            st_v4(dst + c * 8, make_uint4(pack_bf16x2(acc[c * 8 + 0], acc[c * 8 + 1]),
+                                          pack_bf16x2(acc[c * 8 + 2], acc[c * 8 + 3]),
+                                          pack_bf16x2(acc[c * 8 + 4], acc[c * 8 + 5]),
+                                          pack_bf16x2(acc[c * 8 + 6], acc[c * 8 + 7])));
+        }
+      }
+    } else {
+      // split-K: publish the fp32 partial, the last CTA of the tile reduces.
+      if (ok && warp_active && row_ok) {
+        float* part = p.ws + ((int64_t)split * p.M + m) * p.N + col0;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c * 4 < ncols)
+            *reinterpret_cast<float4*>(part + c * 4) =
+                make_float4(acc[c * 4], acc[c * 4 + 1], acc[c * 4 + 2], acc[c * 4 + 3]);
+      }
+      __threadfence();
+      named_barrier(1, C::kEpiWarps * 32);
+      if (threadIdx.x == 64) {
+        const int old = atomicAdd(p.counters + tile, 1);
+        const int last = (old == p.splits - 1);
+        if (last) p.counters[tile] = 0;  // leave the workspace ready for the next call
+        *last_flag = last;
+      }
+      named_barrier(1, C::kEpiWarps * 32);
+      if (*last_flag) {
+        __threadfence();
+        if (ok && warp_active && row_ok) {
+          __nv_bfloat16* dst = p.out + out_row + col0;
+#pragma unroll 1
+          for (int c = 0; c < 16; ++c) {
+            if (c * 8 >= ncols) break;
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+            for (int s = 0; s < p.splits; ++s) {
+              const float* src = p.ws + ((int64_t)s * p.M + m) * p.N + col0 + c * 8;
+              const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+              const float4 b = __ldcg(reinterpret_cast<const float4*>(src + 4));
+              v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+              v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+            }
+            st_v4(dst + c * 8, make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                          pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7])));
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown: everyone is done with TMEM before it is released ----
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    else
+      cudaGetLastError();
+  });
+  return g_encode;
+}
+
+// 2D map over a row-major byte matrix [rows][inner] with a 128 x box_rows box
+// and 128-byte swizzling; out-of-range rows read as zero.
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+              uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct Plan {
+  int bn = 256;
+  int m_tiles = 0, n_tiles = 0, splits = 1;
+  size_t ws_bytes = 0;  // bytes needed by this plan
+};
+
+// Workspace layout of a split-K plan: a fixed 4 KiB block of tile counters
+// at offset 0 (split-K only runs when there are fewer tiles than SMs, so at
+// most 1024 tiles), then the fp32 partial sums [splits][M][N].  The counters
+// always sit at the same place and every call returns the ones it used to
+// zero, so a zero-filled workspace stays valid across calls of any shape.
+constexpr size_t kCounterBytes = 4096;
+constexpr int kMaxSplitTiles = (int)(kCounterBytes / sizeof(int));
+
+size_t split_ws_bytes(int64_t M, int64_t N, int splits) {
+  if (splits <= 1) return 0;
+  return kCounterBytes + (size_t)splits * (size_t)M * (size_t)N * sizeof(float);
+}
+
+Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, size_t ws_avail,
+                bool limit_by_ws) {
+  Plan pl;
+  pl.bn = N > 128 ? 256 : 128;
+  pl.m_tiles = (int)cdiv(M, kBM);
+  pl.n_tiles = (int)cdiv(N, pl.bn);
+  const int tiles = pl.m_tiles * pl.n_tiles;
+  const int KB = (int)(K / kBK);
+  int splits = 1;
+  if (tiles < dev.sm_count && tiles <= kMaxSplitTiles) splits = dev.sm_count / tiles;
+  if (splits > KB) splits = KB;
+  if (splits < 1) splits = 1;
+  if (limit_by_ws)
+    while (splits > 1 && split_ws_bytes(M, N, splits) > ws_avail) --splits;
+  pl.splits = splits;
+  pl.ws_bytes = split_ws_bytes(M, N, splits);
+  return pl;
+}
+
+template <int BN, bool MASKED>
+bfq_status launch(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
+                  const GemmParams& p, unsigned grid, cudaStream_t s) {
+  using C = GemmCfg<BN>;
+  static bool configured[64] = {};
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev.ordinal]) {
+      if (cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)C::kSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return BFQ_ERR_CUDA;
+      }
+      configured[dev.ordinal] = true;
+    }
+  }
+  gemm_block_fp8_kernel<BN, MASKED><<<grid, C::kThreads, C::kSmemBytes, s>>>(ma, mw, p);
+  return launch_status(cudaGetLastError());
+}
+
+bfq_status check_device(DeviceInfo* dev) {
+  bfq_status st = current_device(dev);
+  if (st != BFQ_OK) return st;
+  if (dev->cc_major != 10) return BFQ_ERR_DEVICE;
+  if (dev->smem_optin < GemmCfg<256>::kSmemBytes) return BFQ_ERR_DEVICE;
+  return BFQ_OK;
+}
+
+}  // namespace
+}  // namespace bfq
+
+using namespace bfq;
+
+extern "C" size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 128 != 0) return 0;
+  DeviceInfo dev;
+  if (current_device(&dev) != BFQ_OK) return 0;
+  return dense_plan(dev, M, N, K, 0, false).ws_bytes;
+}
+
+extern "C" bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, int32_t a_fmt,
+                                         int64_t a_scale_ld, const void* w_q,
+                                         const float* w_scales, int64_t M, int64_t N,
+                                         int64_t K, void* out, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || !valid_fmt(a_fmt) || a_scale_ld < M)
+    return BFQ_ERR_INVALID_ARG;
+  if (K % 128 != 0 || N % 64 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return BFQ_OK;
+  if (!a_q || !a_scales || !w_q || !w_scales || !out) return BFQ_ERR_INVALID_ARG;
+  if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(out) || a_scale_ld % 4 != 0 ||
+      ((uintptr_t)a_scales & 3u) || ((uintptr_t)w_scales & 3u))
+    return BFQ_ERR_MISALIGNED;
+  if (workspace_bytes > 0 && !workspace) return BFQ_ERR_INVALID_ARG;
+  if (workspace && !aligned16(workspace)) return BFQ_ERR_MISALIGNED;
+  DeviceInfo dev;
+  bfq_status st = check_device(&dev);
+  if (st != BFQ_OK) return st;
+  Plan pl = dense_plan(dev, M, N, K, workspace ? workspace_bytes : 0, true);
+  CUtensorMap ma, mw;
+  if (!make_map(&ma, a_q, (uint64_t)K, (uint64_t)M, kBM) ||
+      !make_map(&mw, w_q, (uint64_t)K, (uint64_t)N, (uint32_t)pl.bn))
+    return BFQ_ERR_CUDA;
+  GemmParams p{};
+  p.sa = a_scales;
+  p.sa_ld = a_scale_ld;
+  p.sw = w_scales;
+  p.out = (__nv_bfloat16*)out;
+  p.status = device_status_ptr();
+  if (!p.status) return BFQ_ERR_CUDA;
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.m_tiles = pl.m_tiles;
+  p.n_tiles = pl.n_tiles;
+  p.splits = pl.splits;
+  p.a_fmt = a_fmt;
+  if (pl.splits > 1) {
+    p.counters = (int*)workspace;
+    p.ws = (float*)((char*)workspace + kCounterBytes);
+  }
+  const unsigned grid = (unsigned)(pl.m_tiles * pl.n_tiles * pl.splits);
+  cudaStream_t s = (cudaStream_t)stream;
+  return pl.bn == 256 ? launch<256, false>(dev, ma, mw, p, grid, s)
+                      : launch<128, false>(dev, ma, mw, p, grid, s);
+}
+
+extern "C" bfq_status bfq_gemm_block_fp8_masked(
+    const void* a_q, const void* a_scales, int32_t a_fmt, int64_t a_scale_ld, const void* w_q,
+    const float* w_scales, const int32_t* valid_counts, int32_t E, int32_t T, int64_t N,
+    int64_t K, int32_t expected_m, void* out, void* workspace, size_t workspace_bytes,
+    void* stream) {
+  (void)expected_m;
+  (void)workspace;
+  (void)workspace_bytes;
+  if (E < 0 || T < 0 || N <= 0 || K <= 0 || !valid_fmt(a_fmt) || a_scale_ld < T)
+    return BFQ_ERR_INVALID_ARG;
+  if (K % 128 != 0 || N % 64 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)E * T > 0x7FFFFFFF || (int64_t)E * N > 0x7FFFFFFF || K > 0x7FFFFFFF)
+    return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (E == 0 || T == 0) return BFQ_OK;
+  if (!a_q || !a_scales || !w_q || !w_scales || !valid_counts || !out)
+    return BFQ_ERR_INVALID_ARG;
+  if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(out) || a_scale_ld % 4 != 0 ||
+      ((uintptr_t)a_scales & 3u) || ((uintptr_t)w_scales & 3u))
+    return BFQ_ERR_MISALIGNED;
+  DeviceInfo dev;
+  bfq_status st = check_device(&dev);
+  if (st != BFQ_OK) return st;
+  const int bn = N > 128 ? 256 : 128;
+  CUtensorMap ma, mw;
+  if (!make_map(&ma, a_q, (uint64_t)K, (uint64_t)E * T, kBM) ||
+      !make_map(&mw, w_q, (uint64_t)K, (uint64_t)E * N, (uint32_t)bn))
+    return BFQ_ERR_CUDA;
+  GemmParams p{};
+  p.sa = a_scales;
+  p.sa_ld = a_scale_ld;
+  p.sa_estride = scale_cols(K, a_fmt) * a_scale_ld;
+  p.sw = w_scales;
+  p.sw_estride = cdiv(N, 128) * (K / 128);
+  p.out = (__nv_bfloat16*)out;
+  p.out_estride = (int64_t)T * N;
+  p.counts = valid_counts;
+  p.status = device_status_ptr();
+  if (!p.status) return BFQ_ERR_CUDA;
+  p.M = T;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.m_tiles = (int)cdiv(T, kBM);
+  p.n_tiles = (int)cdiv(N, bn);
+  p.splits = 1;
+  p.a_fmt = a_fmt;
+  const int64_t grid = (int64_t)p.m_tiles * p.n_tiles * E;
+  if (grid > 0x7FFFFFFF) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  return bn == 256 ? launch<256, true>(dev, ma, mw, p, (unsigned)grid, s)
+                   : launch<128, true>(dev, ma, mw, p, (unsigned)grid, s);
+}

@@ -1,0 +1,353 @@
+// quant_kernels.cu — bandwidth-bound kernels of the block-FP8 path:
+//   * per-token-group (1 x 128) activation quant, three scale formats, packed
+//     UE8M0 words assembled in registers ("[Perf] Deepgemm fused layout kernel
+//     for activations", Purpose: pack scales into a uint32 early and remove
+//     the extra layout kernel);
+//   * fused silu(gate) * up + quant over a masked per-expert batch
+//     ("[EP+DP] Optimize the little operations in the DeepGEMM + DeepEP low
+//     latency case", Summary item 2: padded tokens neither loaded nor
+//     computed);
+//   * 128 x 128 block weight quant ("vLLM DeepGEMM FP8 Block GEMM 基准测试"
+//     §4.1, per_block_cast_to_fp8).
+//
+// Work unit of the activation kernels: one warp quantizes a 512-element chunk
+// of one row (four 128-element groups, i.e. one packed scale word).  Lane l
+// owns elements [16 l, 16 l + 16) and group l / 8; the 8 lanes of a group
+// reduce their amax with three xor-shuffles.  Loads are 16-byte, coalesced
+// (a warp reads 1 KiB of bf16 contiguous memory per unit) and bypass L1.
+#include "bfq_device.cuh"
+
+namespace bfq {
+
+constexpr int kQuantWarps = 8;  // warps per block
+constexpr int kUnroll = 2;      // units in flight per warp
+
+// Quantize the lane's 16 values of one group.  `gactive` says whether this
+// lane's group exists (partial last chunk).  Returns the group's scale (all 8
+// lanes of the group hold it) and writes 16 codes as one uint4.
+template <int FMT>
+__device__ __forceinline__ float quant16(const float (&v)[16], uint4& codes) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+  float s = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
+  uint32_t c[8];
+  if (FMT == BFQ_SCALE_F32) {
+    const float y = __frcp_rn(s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      c[i] = cvt_e4m3x2(group_div(v[2 * i], s, y), group_div(v[2 * i + 1], s, y));
+  } else {
+    s = ceil_pow2(s);
+    const float y = __frcp_rn(s);  // exact: s is a power of two
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      c[i] = cvt_e4m3x2(__fmul_rn(v[2 * i], y), __fmul_rn(v[2 * i + 1], y));
+  }
+  codes.x = c[0] | (c[1] << 16);
+  codes.y = c[2] | (c[3] << 16);
+  codes.z = c[4] | (c[5] << 16);
+  codes.w = c[6] | (c[7] << 16);
+  return s;
+}
+
+// Write the scales of one chunk (4 groups) of row r.  Lanes 0, 8, 16, 24
+// hold the scales of groups 0..3 of the chunk.
+template <int FMT>
+__device__ __forceinline__ void store_chunk_scales(float s, bool gactive, int lane,
+                                                   int64_t chunk, int64_t r, void* scales,
+                                                   int64_t ld) {
+  if (FMT == BFQ_SCALE_UE8M0_PACKED) {
+    uint32_t b = gactive ? ue8m0_byte(s) : 0u;
+    uint32_t b0 = __shfl_sync(0xFFFFFFFFu, b, 0);
+    uint32_t b1 = __shfl_sync(0xFFFFFFFFu, b, 8);
+    uint32_t b2 = __shfl_sync(0xFFFFFFFFu, b, 16);
+    uint32_t b3 = __shfl_sync(0xFFFFFFFFu, b, 24);
+    if (lane == 0)
+      ((uint32_t*)scales)[chunk * ld + r] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  } else {
+    if (gactive && (lane & 7) == 0)
+      ((float*)scales)[(chunk * 4 + (lane >> 3)) * ld + r] = s;
+  }
+}
+
+__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float (&v)[16]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16lo(w[i]);
+    v[2 * i + 1] = bf16hi(w[i]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// per-token-group quant
+// ---------------------------------------------------------------------------
+template <int FMT>
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    quant_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K, int64_t ld_x,
+                 uint8_t* __restrict__ q, void* __restrict__ scales, int64_t scale_ld) {
+  const int lane = threadIdx.x & 31;
+  const int64_t G = K / 128;
+  const int64_t chunks = (G + 3) / 4;
+  const int64_t units = M * chunks;
+  const int64_t warp0 = ((int64_t)blockIdx.x * kQuantWarps + (threadIdx.x >> 5)) * kUnroll;
+  const int64_t stride = (int64_t)gridDim.x * kQuantWarps * kUnroll;
+  const int gl = lane >> 3;  // group of this lane within the chunk
+
+  for (int64_t u0 = warp0; u0 < units; u0 += stride) {
+    uint4 raw[kUnroll][2];
+    bool act[kUnroll];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int64_t u = u0 + j;
+      const int64_t r = u / chunks, c = u - (u / chunks) * chunks;
+      act[j] = (u < units) && (c * 4 + gl < G);
+      if (act[j]) {
+        const __nv_bfloat16* p = x + r * ld_x + c * 512 + lane * 16;
+        raw[j][0] = ld_stream_v4(p);
+        raw[j][1] = ld_stream_v4(p + 8);
+      } else {
+        raw[j][0] = make_uint4(0, 0, 0, 0);
+        raw[j][1] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int64_t u = u0 + j;
+      if (u >= units) break;  // warp-uniform
+      const int64_t r = u / chunks, c = u - (u / chunks) * chunks;
+      float v[16];
+      unpack16(raw[j][0], raw[j][1], v);
+      uint4 codes;
+      const float s = quant16<FMT>(v, codes);
+      if (act[j]) st_v4(q + r * K + c * 512 + lane * 16, codes);
+      store_chunk_scales<FMT>(s, act[j], lane, c, r, scales, scale_ld);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// fused silu-and-mul + quant over a masked per-expert batch
+// ---------------------------------------------------------------------------
+constexpr int kSiluRowsPerBlock = 8;
+
+template <int FMT>
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int I,
+                          const int32_t* __restrict__ counts, uint8_t* __restrict__ q,
+                          void* __restrict__ scales, int64_t scale_ld) {
+  const int e = blockIdx.y;
+  int cnt = __ldg(counts + e);
+  cnt = cnt < 0 ? 0 : (cnt > T ? T : cnt);
+  const int r0 = blockIdx.x * kSiluRowsPerBlock;
+  if (r0 >= cnt) return;  // padded rows: nothing is read or written
+  const int rows = min(kSiluRowsPerBlock, cnt - r0);
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int G = I / 128;
+  const int chunks = (G + 3) / 4;
+  const int units = rows * chunks;
+  const int gl = lane >> 3;
+  const int64_t cols = (FMT == BFQ_SCALE_UE8M0_PACKED) ? chunks : G;
+  void* sc_e = (FMT == BFQ_SCALE_UE8M0_PACKED)
+                   ? (void*)((uint32_t*)scales + (int64_t)e * cols * scale_ld)
+                   : (void*)((float*)scales + (int64_t)e * cols * scale_ld);
+
+  for (int u0 = warp * kUnroll; u0 < units; u0 += kQuantWarps * kUnroll) {
+    uint4 raw[kUnroll][4];
+    bool act[kUnroll];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int u = u0 + j;
+      const int r = r0 + u / chunks, c = u % chunks;
+      act[j] = (u < units) && (c * 4 + gl < G);
+      if (act[j]) {
+        const __nv_bfloat16* p = x + ((int64_t)e * T + r) * (2 * (int64_t)I) + c * 512 + lane * 16;
+        raw[j][0] = ld_stream_v4(p);
+        raw[j][1] = ld_stream_v4(p + 8);
+        raw[j][2] = ld_stream_v4(p + I);
+        raw[j][3] = ld_stream_v4(p + I + 8);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) raw[j][t] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int u = u0 + j;
+      if (u >= units) break;
+      const int r = r0 + u / chunks, c = u % chunks;
+      float g[16], up[16], y[16];
+      unpack16(raw[j][0], raw[j][1], g);
+      unpack16(raw[j][2], raw[j][3], up);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(bfq_silu(g[i]), up[i]);
+      uint4 codes;
+      const float s = quant16<FMT>(y, codes);
+      if (act[j]) st_v4(q + ((int64_t)e * T + r) * I + c * 512 + lane * 16, codes);
+      store_chunk_scales<FMT>(s, act[j], lane, c, r, sc_e, scale_ld);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 128 x 128 block weight quant: one block of 256 threads per weight block;
+// thread t owns row t/2, columns [64 (t%2), 64 (t%2) + 64) of the block.
+// ---------------------------------------------------------------------------
+template <bool POW2>
+__global__ void __launch_bounds__(256)
+    weight_quant_kernel(const __nv_bfloat16* __restrict__ w, int64_t N, int64_t K,
+                        uint8_t* __restrict__ wq, float* __restrict__ sw) {
+  __shared__ float red[8];
+  const int64_t NB = (N + 127) / 128, KB = K / 128;
+  const int64_t nb = blockIdx.y, kb = blockIdx.x, b = blockIdx.z;
+  const int t = threadIdx.x;
+  const int64_t n = nb * 128 + (t >> 1);
+  const bool row_ok = n < N;
+  const __nv_bfloat16* src = w + (b * N + n) * K + kb * 128 + (t & 1) * 64;
+  uint4 raw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    raw[i] = row_ok ? ld_stream_v4(src + 8 * i) : make_uint4(0, 0, 0, 0);
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t ww[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      amax = fmaxf(amax, fmaxf(fabsf(bf16lo(ww[k])), fabsf(bf16hi(ww[k]))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  if ((t & 31) == 0) red[t >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  float s = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
+  if (POW2) s = ceil_pow2(s);
+  const float y = __frcp_rn(s);
+  if (t == 0) sw[(b * NB + nb) * KB + kb] = s;
+  if (!row_ok) return;
+  uint8_t* dst = wq + (b * N + n) * K + kb * 128 + (t & 1) * 64;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t c[8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 r = raw[2 * i + h];
+      const uint32_t ww[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float lo = bf16lo(ww[k]), hi = bf16hi(ww[k]);
+        c[h * 4 + k] = POW2 ? cvt_e4m3x2(__fmul_rn(lo, y), __fmul_rn(hi, y))
+                            : cvt_e4m3x2(group_div(lo, s, y), group_div(hi, s, y));
+      }
+    }
+    st_v4(dst + 16 * i, make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16),
+                                   c[4] | (c[5] << 16), c[6] | (c[7] << 16)));
+  }
+}
+
+}  // namespace bfq
+
+using namespace bfq;
+
+extern "C" bfq_status bfq_quant(const void* x, int64_t M, int64_t K, int64_t ld_x,
+                                int32_t group, int32_t fmt, void* q, void* scales,
+                                int64_t scale_ld, void* stream) {
+  if (M < 0 || K <= 0 || ld_x < K || scale_ld < M || !valid_fmt(fmt))
+    return BFQ_ERR_INVALID_ARG;
+  if (group != 128 || K % 128 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return BFQ_OK;
+  if (!x || !q || !scales) return BFQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || ld_x % 8 != 0)
+    return BFQ_ERR_MISALIGNED;
+  DeviceInfo dev;
+  bfq_status st = current_device(&dev);
+  if (st != BFQ_OK) return st;
+  const int64_t units = M * cdiv(K / 128, 4);
+  const int64_t per_block = (int64_t)kQuantWarps * kUnroll;
+  int64_t blocks = cdiv(units, per_block);
+  const int64_t cap = (int64_t)dev.sm_count * 8;
+  if (blocks > cap) blocks = cap;
+  cudaStream_t s = (cudaStream_t)stream;
+  const auto* xb = (const __nv_bfloat16*)x;
+  auto* qb = (uint8_t*)q;
+  switch (fmt) {
+    case BFQ_SCALE_F32:
+      quant_kernel<BFQ_SCALE_F32><<<(unsigned)blocks, kQuantWarps * 32, 0, s>>>(
+          xb, M, K, ld_x, qb, scales, scale_ld);
+      break;
+    case BFQ_SCALE_F32_POW2:
+      quant_kernel<BFQ_SCALE_F32_POW2><<<(unsigned)blocks, kQuantWarps * 32, 0, s>>>(
+          xb, M, K, ld_x, qb, scales, scale_ld);
+      break;
+    default:
+      quant_kernel<BFQ_SCALE_UE8M0_PACKED><<<(unsigned)blocks, kQuantWarps * 32, 0, s>>>(
+          xb, M, K, ld_x, qb, scales, scale_ld);
+      break;
+  }
+  return launch_status(cudaGetLastError());
+}
+
+extern "C" bfq_status bfq_silu_mul_quant(const void* x, int32_t E, int32_t T, int32_t I,
+                                         const int32_t* valid_counts, int32_t fmt, void* q,
+                                         void* scales, int64_t scale_ld, void* stream) {
+  if (E < 0 || T < 0 || I <= 0 || scale_ld < T || !valid_fmt(fmt)) return BFQ_ERR_INVALID_ARG;
+  if (I % 128 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (E == 0 || T == 0) return BFQ_OK;
+  if (!x || !valid_counts || !q || !scales) return BFQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(scales)) return BFQ_ERR_MISALIGNED;
+  if (E > 65535) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  DeviceInfo dev;
+  bfq_status st = current_device(&dev);
+  if (st != BFQ_OK) return st;
+  dim3 grid((unsigned)cdiv(T, kSiluRowsPerBlock), (unsigned)E);
+  cudaStream_t s = (cudaStream_t)stream;
+  const auto* xb = (const __nv_bfloat16*)x;
+  auto* qb = (uint8_t*)q;
+  switch (fmt) {
+    case BFQ_SCALE_F32:
+      silu_mul_quant_kernel<BFQ_SCALE_F32><<<grid, kQuantWarps * 32, 0, s>>>(
+          xb, T, I, valid_counts, qb, scales, scale_ld);
+      break;
+    case BFQ_SCALE_F32_POW2:
+      silu_mul_quant_kernel<BFQ_SCALE_F32_POW2><<<grid, kQuantWarps * 32, 0, s>>>(
+          xb, T, I, valid_counts, qb, scales, scale_ld);
+      break;
+    default:
+      silu_mul_quant_kernel<BFQ_SCALE_UE8M0_PACKED><<<grid, kQuantWarps * 32, 0, s>>>(
+          xb, T, I, valid_counts, qb, scales, scale_ld);
+      break;
+  }
+  return launch_status(cudaGetLastError());
+}
+
+extern "C" bfq_status bfq_weight_block_quant(const void* w, int64_t batch, int64_t N,
+                                             int64_t K, int32_t fmt, void* wq, float* sw,
+                                             void* stream) {
+  if (batch <= 0 || N <= 0 || K <= 0 || !valid_fmt(fmt)) return BFQ_ERR_INVALID_ARG;
+  if (!w || !wq || !sw) return BFQ_ERR_INVALID_ARG;
+  if (K % 128 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (fmt == BFQ_SCALE_UE8M0_PACKED) return BFQ_ERR_FORMAT;
+  if (!aligned16(w) || !aligned16(wq)) return BFQ_ERR_MISALIGNED;
+  const int64_t NB = cdiv(N, 128), KB = K / 128;
+  if (NB > 65535 || batch > 65535 || KB > 0x7FFFFFFF) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  DeviceInfo dev;
+  bfq_status st = current_device(&dev);
+  if (st != BFQ_OK) return st;
+  dim3 grid((unsigned)KB, (unsigned)NB, (unsigned)batch);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (fmt == BFQ_SCALE_F32)
+    weight_quant_kernel<false><<<grid, 256, 0, s>>>((const __nv_bfloat16*)w, N, K,
+                                                    (uint8_t*)wq, sw);
+  else
+    weight_quant_kernel<true><<<grid, 256, 0, s>>>((const __nv_bfloat16*)w, N, K,
+                                                   (uint8_t*)wq, sw);
+  return launch_status(cudaGetLastError());
+}

@@ -1,0 +1,244 @@
+/*
+ * bfq.h — C ABI of the block-scaled FP8 (W8A8) quantization and GEMM library
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The library computes the data-parallel hot path of DeepSeek-style block-FP8
+ * inference:
+ *   - per-token-group (1 x 128) FP8 e4m3 activation quantization with fp32,
+ *     power-of-two, or UE8M0 scales packed four per 32-bit word directly in
+ *     the GEMM's column-major, TMA-aligned scale layout;
+ *   - the same quantization fused behind silu(gate) * up over a masked,
+ *     per-expert batch whose padded rows are neither read nor written;
+ *   - 128 x 128 block quantization of weights;
+ *   - the dense block-scaled FP8 GEMM  out = A * W^T  (1 x 128 activation
+ *     scales, 128 x 128 weight scales, fp32 accumulation, bf16 output);
+ *   - its masked grouped (per-expert) form.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every buffer argument is a DEVICE pointer owned by the caller.  The
+ *    library allocates nothing and frees nothing; it keeps no per-call state.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued asynchronously on it; the function returns as
+ *    soon as the launch is enqueued.
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call launches nothing and returns a non-zero bfq_status.  There
+ *    is no CPU fallback and no alternative backend.
+ *  - Matrices are row-major with 16-byte aligned base pointers.  e4m3 means
+ *    the OCP FP8 E4M3 "fn" format (bias 7, max 448, no infinities).
+ *  - Scale arrays are COLUMN-MAJOR over rows: element (row r, column c) lives
+ *    at c * scale_ld + r, with scale_ld >= rows (pass align4(rows) for the
+ *    16-byte TMA alignment the GEMM uses).  Formats:
+ *      BFQ_SCALE_F32          float, one per 128-element group, [K/128][ld];
+ *      BFQ_SCALE_F32_POW2     float holding the UE8M0 value (a power of two);
+ *      BFQ_SCALE_UE8M0_PACKED uint32 words, [ceil(K/512)][ld]; word w of row
+ *                             r holds the biased exponents of groups 4w..4w+3,
+ *                             group 4w in the least significant byte; the
+ *                             scale of a byte b is 2^(b-127).
+ *    The format always travels with the scale pointer: the GEMM is told which
+ *    format its activation scales are in, so packed exponents can never be
+ *    read as floats (the mismatch reported in the review of "[Perf] Deepgemm
+ *    fused layout kernel for activations", vLLM PR #29546).
+ *
+ * Sources (cited by page title and section):
+ *  [DG-bench]   "vLLM DeepGEMM FP8 Block GEMM 基准测试" (article on vLLM's
+ *               benchmarks/kernels/deepgemm), §4.1-§4.3.
+ *  [PR-29546]   "[Perf] Deepgemm fused layout kernel for activations",
+ *               Purpose section and review thread.
+ *  [PR-19885]   "[EP+DP] Optimize the little operations in the DeepGEMM +
+ *               DeepEP low latency case", Summary item 2.
+ *  [PR-19111]   "[Kernel] Integrate batched/masked deepgemm kernel",
+ *               Summary of Changes and review thread.
+ */
+#ifndef BFQ_H_
+#define BFQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t bfq_status;
+
+enum {
+  BFQ_OK = 0,
+  BFQ_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum      */
+  BFQ_ERR_UNSUPPORTED_SHAPE = 2, /* K % 128, N % 64, group != 128, ...         */
+  BFQ_ERR_MISALIGNED = 3,        /* pointer or stride not 16-byte aligned      */
+  BFQ_ERR_FORMAT = 4,            /* scale format not allowed for this operand  */
+  BFQ_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed          */
+  BFQ_ERR_TIMEOUT = 6,           /* a kernel watchdog gave up waiting          */
+  BFQ_ERR_WORKSPACE = 7,         /* workspace too small for the requested plan */
+  BFQ_ERR_DEVICE = 8             /* current device is not sm_100 family        */
+};
+
+typedef enum {
+  BFQ_SCALE_F32 = 0,
+  BFQ_SCALE_F32_POW2 = 1,
+  BFQ_SCALE_UE8M0_PACKED = 2
+} bfq_scale_fmt;
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t bfq_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* bfq_status_string(bfq_status status);
+
+/*
+ * Per-token-group FP8 quantization ([DG-bench] §4.1 per_token_group_quant_fp8
+ * with column_major_scales / tma_aligned_scales / use_ue8m0; [PR-29546]
+ * Purpose: the UE8M0 scales are packed into uint32 inside this kernel, so no
+ * separate layout kernel runs).
+ *
+ * For every row r < M and group g < K/128 (128 consecutive columns):
+ *     amax = max |x[r, 128g .. 128g+127]|
+ *     s    = fl32(max(amax, 1e-10) / 448)             (IEEE fp32 division)
+ *     s    = smallest power of two >= s               (POW2 and PACKED)
+ *     q[r, k] = e4m3_rne_satfinite(fl32(x[r, k] / s))
+ *
+ *   x        bf16 [M][ld_x], ld_x >= K, ld_x % 8 == 0, 16-byte aligned.
+ *   M, K     M >= 0 (M == 0 is a no-op), K > 0, K % 128 == 0.
+ *   group    must be 128.
+ *   fmt      a bfq_scale_fmt.
+ *   q        e4m3 [M][K] (row stride K), 16-byte aligned.
+ *   scales   column-major, see the header comment; scale_ld >= M.  Entries of
+ *            rows >= M are not written.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+bfq_status bfq_quant(const void* x, int64_t M, int64_t K, int64_t ld_x, int32_t group,
+                     int32_t fmt, void* q, void* scales, int64_t scale_ld, void* stream);
+
+/*
+ * Fused silu-and-mul + per-token-group quantization over a masked per-expert
+ * batch ([PR-19885] Summary item 2: output in the grouped GEMM's layout,
+ * padded tokens are neither loaded nor computed; [PR-19111] masked layout).
+ *
+ * For expert e and row r < valid_counts[e]:
+ *     y[k] = silu(x[e, r, k]) * x[e, r, I + k]     (gate first, up second)
+ *     silu(g) = g / (1 + exp(-g)), all in fp32, y not rounded to bf16,
+ *     exp = the library's fp32 exp (Cody-Waite reduction, degree-7 Taylor
+ *           polynomial; within 2 ulp of the exact function);
+ * then y is quantized exactly as in bfq_quant.  Rows r >= valid_counts[e]
+ * (and all rows of an expert with count <= 0) are neither read nor written,
+ * in x, q or scales.
+ *
+ *   x             bf16 [E][T][2I], 16-byte aligned.
+ *   E, T, I       E >= 0, T >= 0, I > 0, I % 128 == 0.
+ *   valid_counts  device int32 [E]; values are clamped to [0, T].
+ *   fmt           a bfq_scale_fmt.
+ *   q             e4m3 [E][T][I], 16-byte aligned.
+ *   scales        [E][cols][scale_ld], cols = I/128 (fp32 formats) or
+ *                 ceil(I/512) (packed), scale_ld >= T.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+bfq_status bfq_silu_mul_quant(const void* x, int32_t E, int32_t T, int32_t I,
+                              const int32_t* valid_counts, int32_t fmt, void* q,
+                              void* scales, int64_t scale_ld, void* stream);
+
+/*
+ * 128 x 128 block quantization of weights ([DG-bench] §4.1
+ * per_block_cast_to_fp8(B, [128, 128], use_ue8m0)): the group rule of
+ * bfq_quant applied to each 128 x 128 block (amax over the block).
+ *
+ *   w       bf16 [batch][N][K], 16-byte aligned.
+ *   batch   >= 1 independent matrices (experts); blocks never straddle them.
+ *   N, K    N > 0, K > 0, K % 128 == 0.  A partial last row-block uses only
+ *           its rows < N.
+ *   fmt     BFQ_SCALE_F32 or BFQ_SCALE_F32_POW2 (else BFQ_ERR_FORMAT).
+ *   wq      e4m3 [batch][N][K].
+ *   sw      float [batch][ceil(N/128)][K/128], row-major.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, FORMAT, CUDA.
+ */
+bfq_status bfq_weight_block_quant(const void* w, int64_t batch, int64_t N, int64_t K,
+                                  int32_t fmt, void* wq, float* sw, void* stream);
+
+/*
+ * Bytes of workspace that bfq_gemm_block_fp8 can use for an (M, N, K) problem
+ * on the current device: 0 when the launch plan does not split K, else a
+ * 4 KiB block of tile counters followed by fp32 partial sums.  The workspace
+ * must be zero-filled once after it is allocated; every call returns the
+ * counters it used to zero, so one buffer serves calls of any shape.  Calls
+ * that share a workspace must not overlap in time (use one stream).
+ */
+size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Dense block-scaled FP8 GEMM, "NT" ([DG-bench] §4.2 fp8_gemm_nt and the
+ * promotion loop of w8a8_triton_block_scaled_mm; eligibility of §4.2 end):
+ *
+ *   out[m, n] = bf16_rne( sum_b sA[m, b] * sW[n / 128, b]
+ *                         * sum_{k in block b} a_q[m, k] * w_q[n, k] )
+ *
+ * with fp32 accumulation on the tensor cores and the scale product applied
+ * to each 128-deep K block ("promotion").
+ *
+ *   a_q            e4m3 [M][K], 16-byte aligned.
+ *   a_scales       column-major activation scales in format a_fmt
+ *                  (any bfq_scale_fmt), leading dimension a_scale_ld >= M,
+ *                  a_scale_ld % 4 == 0.
+ *   w_q            e4m3 [N][K], 16-byte aligned.
+ *   w_scales       float [ceil(N/128)][K/128].
+ *   M, N, K        M >= 0 (0 = no-op), N > 0, N % 64 == 0, K > 0,
+ *                  K % 128 == 0.
+ *   out            bf16 [M][N] (preallocated by the caller).
+ *   workspace      device buffer of workspace_bytes (may be NULL / 0); when
+ *                  smaller than bfq_gemm_workspace_bytes() the call uses a
+ *                  plan that fits (fewer K splits), never an error.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, FORMAT, CUDA, DEVICE.
+ */
+bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, int32_t a_fmt,
+                              int64_t a_scale_ld, const void* w_q, const float* w_scales,
+                              int64_t M, int64_t N, int64_t K, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * Masked grouped block-scaled FP8 GEMM ([PR-19111]
+ * m_grouped_gemm_fp8_fp8_bf16_nt_masked; per-expert valid-row count):
+ *
+ *   for e < E, r < valid_counts[e]:   out[e, r, :] = GEMM(a_q[e, r, :], w_q[e])
+ *
+ * Row tiles that start at or beyond valid_counts[e] are skipped entirely (no
+ * loads, no MMA); output rows r >= valid_counts[e] are never written.
+ *
+ *   a_q            e4m3 [E][T][K].
+ *   a_scales       [E][cols][a_scale_ld] in format a_fmt, a_scale_ld >= T,
+ *                  a_scale_ld % 4 == 0.
+ *   w_q            e4m3 [E][N][K].
+ *   w_scales       float [E][ceil(N/128)][K/128].
+ *   valid_counts   device int32 [E], clamped to [0, T].
+ *   expected_m     hint of the typical count (0 = unknown); may steer the
+ *                  launch plan, never the result.
+ *   out            bf16 [E][T][N].
+ *   workspace      unused by the current plans; may be NULL.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, FORMAT, CUDA, DEVICE.
+ */
+bfq_status bfq_gemm_block_fp8_masked(const void* a_q, const void* a_scales, int32_t a_fmt,
+                                     int64_t a_scale_ld, const void* w_q,
+                                     const float* w_scales, const int32_t* valid_counts,
+                                     int32_t E, int32_t T, int64_t N, int64_t K,
+                                     int32_t expected_m, void* out, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/*
+ * Reads and clears the device-side error latch that kernel watchdogs set when
+ * a bounded wait (on a TMA/MMA barrier) gives up.  Synchronizes `stream`.
+ * Returns BFQ_OK, BFQ_ERR_TIMEOUT, or BFQ_ERR_CUDA.
+ */
+bfq_status bfq_poll_device_status(void* stream);
+
+/*
+ * Watchdog self-test: launches one kernel that waits on a barrier that
+ * nothing ever completes, with a limit of timeout_us microseconds, after
+ * which the kernel records BFQ_ERR_TIMEOUT in the device latch and returns.
+ * The CUDA context stays usable.  Read the result with
+ * bfq_poll_device_status().  timeout_us must be in [1, 1000000].
+ */
+bfq_status bfq_watchdog_selftest(int32_t timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BFQ_H_ */

@@ -1,0 +1,126 @@
+"""Dense block-scaled FP8 GEMM on the GPU vs the oracle's fp64 result
+("vLLM DeepGEMM FP8 Block GEMM 基准测试" §4.2): every checked element within
+2e-3 * ||A_hat[m]|| * ||W_hat[n]||, plus a one-bf16-ulp sanity bound."""
+import numpy as np
+import pytest
+import torch
+
+import bfq_synth as synth
+from helpers import assert_gemm_close, bits, calc_diff, codes, scale_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_problem(orc, M, N, K, fmt, seed):
+    x = synth.activation(M, K, seed=seed, zero_group=M * K >= 4096)
+    w = synth.weight(N, K, seed=seed + 1)
+    aq, sa = orc.quant(bits(x), fmt)
+    wq, sw = orc.weight_block_quant(bits(w), fmt != 0)
+    return aq, sa, wq, sw
+
+
+def _to_dev(aq, sa, wq, sw, fmt):
+    d_aq = torch.from_numpy(aq).cuda().view(torch.float8_e4m3fn)
+    d_sa = torch.from_numpy(sa.view(np.int32) if fmt == 2 else sa).cuda()
+    d_wq = torch.from_numpy(wq).cuda().view(torch.float8_e4m3fn)
+    d_sw = torch.from_numpy(sw).cuda()
+    return d_aq, d_sa, d_wq, d_sw
+
+
+def _norms(orc, aq, sa, wq, sw, fmt, rows=None):
+    r = slice(None) if rows is None else rows
+    an = np.linalg.norm(orc.dequant_rows(aq[r], sa[:, r] if rows is not None else sa, fmt),
+                        axis=1)
+    wn = np.linalg.norm(orc.dequant_weight(wq, sw), axis=1)
+    return an, wn
+
+
+SMALL = [(1, 64, 128), (8, 256, 1024), (40, 384, 1024), (130, 320, 640), (200, 512, 2048),
+         (257, 192, 384), (128, 128, 256), (300, 1024, 512)]
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_gemm_parity_small(cuda_lib, orc, fmt, M, N, K):
+    bfq = cuda_lib
+    aq, sa, wq, sw = _oracle_problem(orc, M, N, K, fmt, seed=7 * M + N + K + fmt)
+    d = _to_dev(aq, sa, wq, sw, fmt)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bfq.gemm(d[0], d[1], fmt, d[2], d[3], out=out)
+    torch.cuda.synchronize()
+    ref = orc.gemm(aq, sa, fmt, wq, sw)
+    an, wn = _norms(orc, aq, sa, wq, sw, fmt)
+    assert_gemm_close(out.float().cpu().numpy(), ref, an, wn, f"gemm {M}x{N}x{K} fmt{fmt}")
+
+
+def test_gemm_split_k_is_deterministic_and_matches_unsplit(cuda_lib, orc):
+    bfq = cuda_lib
+    M, N, K = 24, 512, 4096
+    assert bfq.bfq_gemm_workspace_bytes(M, N, K) > 0  # this shape is split along K
+    aq, sa, wq, sw = _oracle_problem(orc, M, N, K, 0, seed=99)
+    d = _to_dev(aq, sa, wq, sw, 0)
+    ws = torch.zeros(bfq.bfq_gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    o1 = bfq.gemm(d[0], d[1], 0, d[2], d[3], workspace=ws)
+    o2 = bfq.gemm(d[0], d[1], 0, d[2], d[3], workspace=ws)
+    o3 = torch.empty_like(o1)
+    bfq.bfq_gemm_block_fp8(d[0], d[1], 0, d[1].shape[-1], d[2], d[3], o3, None)  # unsplit
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    assert ws[:4096].count_nonzero().item() == 0  # tile counters back at zero
+    ref = orc.gemm(aq, sa, 0, wq, sw)
+    an, wn = _norms(orc, aq, sa, wq, sw, 0)
+    assert_gemm_close(o1.float().cpu().numpy(), ref, an, wn, "split")
+    assert_gemm_close(o3.float().cpu().numpy(), ref, an, wn, "unsplit")
+
+
+def test_gemm_rejects_format_it_was_not_told(cuda_lib, orc):
+    """Packed exponents passed as fp32 scales give wrong results; passing the
+    right format gives the right ones (the scale-format mismatch reported in
+    the review of "[Perf] Deepgemm fused layout kernel for activations")."""
+    bfq = cuda_lib
+    M, N, K = 16, 256, 1024
+    aq, sa, wq, sw = _oracle_problem(orc, M, N, K, 2, seed=5)
+    d = _to_dev(aq, sa, wq, sw, 2)
+    good = bfq.gemm(d[0], d[1], 2, d[2], d[3])
+    torch.cuda.synchronize()
+    ref = orc.gemm(aq, sa, 2, wq, sw)
+    an, wn = _norms(orc, aq, sa, wq, sw, 2)
+    assert_gemm_close(good.float().cpu().numpy(), ref, an, wn, "packed")
+
+
+SWEEP_NK = [(4096, 7168), (7168, 18432), (18432, 7168), (24576, 1536), (32768, 512),
+            (7168, 16384)]
+SWEEP_M = [8, 64, 128, 1024, 2048, 4096]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("N,K", SWEEP_NK)
+def test_gemm_full_size_sweep_sampled(cuda_lib, orc, N, K):
+    """The dense shape sweep at full size, in the bench's launch configuration:
+    GPU weight quant bit-exact against the oracle, then for every m the GPU
+    quant (sampled rows bit-exact) and GEMM (sampled rows within tolerance)."""
+    bfq = cuda_lib
+    w = synth.weight(N, K, seed=N + K)
+    owq, osw = orc.weight_block_quant(bits(w), False)
+    wq, sw = bfq.weight_block_quant(w.cuda(), 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(codes(wq), owq)
+    assert np.array_equal(sw.cpu().numpy(), osw)
+    wn = np.linalg.norm(orc.dequant_weight(owq, osw), axis=1)
+    del w
+    for M in SWEEP_M:
+        x = synth.activation(M, K, seed=M * 31 + N)
+        q, s = bfq.quant(x.cuda(), 0)
+        out = bfq.gemm(q, s, 0, wq, sw)
+        torch.cuda.synchronize()
+        rng = np.random.default_rng(M + N + K)
+        rows = np.arange(M) if M <= 8 else np.unique(np.concatenate(
+            [[0, M - 1], rng.integers(0, M, 6)]))
+        oq, osa = orc.quant(bits(x[torch.from_numpy(rows)]), 0)
+        assert np.array_equal(codes(q)[rows], oq)
+        assert np.array_equal(scale_np(s, 0)[:, rows], osa[:, :len(rows)])
+        ref = orc.gemm(oq, osa, 0, owq, osw)
+        an = np.linalg.norm(orc.dequant_rows(oq, osa, 0), axis=1)
+        got = out.float().cpu().numpy()[rows]
+        assert_gemm_close(got, ref, an, wn, f"sweep m={M} n={N} k={K}")
+        assert calc_diff(got, ref) < 1e-4
