@@ -176,7 +176,7 @@ SAMPLE_COLS = 1024
 
 def oracle_sample_step():
     """One bounded sample of the workload on the CPU oracle: 8 activation rows
-    against the first 2048 weight rows of each of the 6 (n, k) shapes (weight
+    against the first 1024 weight rows of each of the 6 (n, k) shapes (weight
     block quant of that slice, activation quant, GEMM).  Returns FLOPs done."""
     import numpy as np
 
@@ -241,15 +241,19 @@ def run_reference(args, rank, world):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def build_problem(bfq, torch, dev):
+def build_problem(bfq, torch, dev, only=None):
     import bfq_synth as synth
 
     shapes = []
     for n, k in SWEEP_NK:
+        if only and (only[1], only[2]) != (n, k):
+            continue
         w = synth.weight(n, k, seed=n + k, device=dev)
         wq, sw = bfq.weight_block_quant(w, bfq.SCALE_F32)
         del w
         for m in SWEEP_M:
+            if only and only[0] != m:
+                continue
             x = synth.activation(m, k, seed=m * 31 + n, device=dev)
             q = torch.empty((m, k), dtype=torch.float8_e4m3fn, device=dev)
             s = torch.empty((k // 128, bfq.align4(m)), dtype=torch.float32, device=dev)
@@ -282,6 +286,25 @@ def e2e_step(bfq, torch, shapes, host_x, host_out):
         ho.copy_(sh["out"], non_blocking=True)
 
 
+def timed_launches(bfq, torch, shapes, reps):
+    """Per-launch durations (ms) of quant and GEMM for every shape, measured
+    with CUDA events on the launching stream.  Each repetition first enqueues
+    a short device-side sleep so that the host has queued the whole step
+    before the GPU reaches it: host launch latency cannot show up as kernel
+    time.  The sleep lies outside every event pair."""
+    qt = [[] for _ in shapes]
+    gt = [[] for _ in shapes]
+    for _ in range(reps):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in shapes]
+        torch.cuda._sleep(20_000_000)
+        step(bfq, shapes, ev)
+        torch.cuda.synchronize()
+        for j in range(len(shapes)):
+            qt[j].append(ev[j][0].elapsed_time(ev[j][1]))
+            gt[j].append(ev[j][1].elapsed_time(ev[j][2]))
+    return qt, gt
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
 
@@ -294,7 +317,7 @@ def run_gpu(args, rank, world, local_rank):
     hbm_peak = float(peaks["hbm_gbs"])
     fp8_peak = float(peaks["bf16_tflops"]) * FP8_PER_BF16
 
-    shapes = build_problem(bfq, torch, dev)
+    shapes = build_problem(bfq, torch, dev, args.shape)
     n_shapes = len(shapes)
     flops_step = sum(2 * s["m"] * s["n"] * s["k"] for s in shapes)
 
@@ -305,9 +328,26 @@ def run_gpu(args, rank, world, local_rank):
     for _ in range(args.warmup):
         step(bfq, shapes)
     torch.cuda.synchronize()
+    if args.shape:  # profiling mode: a few eager steps of one shape, no report
+        for _ in range(args.steps):
+            step(bfq, shapes)
+        torch.cuda.synchronize()
+        return 0
 
-    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_shapes)]
-              for _ in range(args.steps)]
+    # the whole step (all launches) as one CUDA graph, replayed K times
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(bfq, shapes)  # warm the capture stream
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            step(bfq, shapes)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
@@ -315,8 +355,8 @@ def run_gpu(args, rank, world, local_rank):
     with ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
                       int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])) as clk:
         start.record()
-        for i in range(args.steps):
-            step(bfq, shapes, events[i])
+        for _ in range(args.steps):
+            graph.replay()
         stop.record()
         torch.cuda.synchronize()
     if dist is not None:
@@ -326,33 +366,37 @@ def run_gpu(args, rank, world, local_rank):
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
+
+    reps = max(3, min(args.steps, 20))
+    qts, gts = timed_launches(bfq, torch, shapes, reps)
     status = bfq.bfq_poll_device_status()
     if status != 0:
         raise RuntimeError(f"device watchdog reported status {status}")
 
-    # per-launch durations (median over the timed steps)
     per_shape = []
     gemm_ms_total = quant_ms_total = 0.0
     for j, sh in enumerate(shapes):
-        qt = [events[i][j][0].elapsed_time(events[i][j][1]) for i in range(args.steps)]
-        gt = [events[i][j][1].elapsed_time(events[i][j][2]) for i in range(args.steps)]
+        qt, gt = qts[j], gts[j]
         gemm_ms_total += sum(gt)
         quant_ms_total += sum(qt)
         m, n, k = sh["m"], sh["n"], sh["k"]
         g_us = statistics.median(gt) * 1e3
         q_us = statistics.median(qt) * 1e3
-        t_roof = max(2.0 * m * n * k / (fp8_peak * 1e12), gemm_alg_bytes(m, n, k) / (hbm_peak * 1e9))
+        t_flop = 2.0 * m * n * k / (fp8_peak * 1e12)
+        t_byte = gemm_alg_bytes(m, n, k) / (hbm_peak * 1e9)
         per_shape.append({
             "m": m, "n": n, "k": k, "gemm_us": round(g_us, 2),
+            "gemm_us_p10": round(sorted(gt)[len(gt) // 10] * 1e3, 2),
+            "gemm_us_p90": round(sorted(gt)[(9 * len(gt)) // 10] * 1e3, 2),
             "tflops": round(pages_tflops(m, n, k, g_us), 1),
             "gbps_pages": round(pages_gbps(m, n, k, g_us), 1),
-            "roofline_frac": round(t_roof * 1e6 / g_us, 3),
-            "bound": "tensor" if 2.0 * m * n * k / (fp8_peak * 1e12) >= gemm_alg_bytes(m, n, k) / (hbm_peak * 1e9) else "hbm",
+            "roofline_frac": round(max(t_flop, t_byte) * 1e6 / g_us, 3),
+            "bound": "tensor" if t_flop >= t_byte else "hbm",
             "quant_us": round(q_us, 2),
             "quant_gbps": round(quant_alg_bytes(m, k) / (q_us * 1e-6) / 1e9, 1),
         })
-    gemm_launch_ms = gemm_ms_total / (args.steps * n_shapes)
-    achieved_tflops = flops_step * args.steps / (gemm_ms_total * 1e-3) / 1e12
+    gemm_launch_ms = gemm_ms_total / (reps * n_shapes)
+    achieved_tflops = flops_step * reps / (gemm_ms_total * 1e-3) / 1e12
     gemm_bytes_avg = sum(gemm_alg_bytes(s["m"], s["n"], s["k"]) for s in shapes) / n_shapes
     t_roof_sum = sum(max(2.0 * s["m"] * s["n"] * s["k"] / (fp8_peak * 1e12),
                          gemm_alg_bytes(s["m"], s["n"], s["k"]) / (hbm_peak * 1e9)) for s in shapes)
@@ -396,6 +440,7 @@ def run_gpu(args, rank, world, local_rank):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "shapes": n_shapes, "act_scales": "fp32 col-major",
                    "weight_scales": "fp32 128x128", "parallelism": f"replicas x{world}",
+                   "timed": "CUDA graph of the whole step (quant + GEMM per shape), replayed",
                    "l2": "no flush: one step streams ~1.2 GB of distinct operands (> 129 MB "
                          "L2) before any shape repeats"},
         "e2e": {"value": world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
@@ -409,8 +454,8 @@ def run_gpu(args, rank, world, local_rank):
                      "peak_source": f"{peak_src} bf16 burst x {FP8_PER_BF16} (fp8:bf16 nominal)",
                      "alg_bytes_per_launch_avg": gemm_bytes_avg,
                      "avg_launch_us": round(gemm_launch_ms * 1e3, 2),
-                     "mixed_frac": round(t_roof_sum * 1e3 / (gemm_ms_total / args.steps), 4)},
-        "quant": {"total_us_per_step": round(quant_ms_total / args.steps * 1e3, 1),
+                     "mixed_frac": round(t_roof_sum * 1e3 / (gemm_ms_total / reps), 4)},
+        "quant": {"total_us_per_step": round(quant_ms_total / reps * 1e3, 1),
                   "hbm_peak_gbs": hbm_peak},
         "clocks": clk.summary(),
         "shapes": per_shape,
@@ -424,8 +469,11 @@ def run_gpu(args, rank, world, local_rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--shape", type=lambda v: tuple(int(t) for t in v.split(",")), default=None,
+                    help="m,n,k of one sweep shape: run only it, eagerly, and print nothing "
+                         "(for profiler captures)")
     ap.add_argument("--impl", choices=["bfq", "reference"], default="bfq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

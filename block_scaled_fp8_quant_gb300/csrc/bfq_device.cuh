@@ -313,6 +313,71 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes delivered as 16
+// register pairs (column 2i in the low half of p[i]), followed by the wait
+// for the load — one asm statement, so no use can precede the data.
+__device__ __forceinline__ void tmem_ld32_pairs_wait(uint32_t taddr, uint64_t (&p)[16]) {
+  asm volatile(
+      "{\n\t.reg .b32 t<32>;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,"
+      "t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "mov.b64 %0, {t0,t1};\n\tmov.b64 %1, {t2,t3};\n\t"
+      "mov.b64 %2, {t4,t5};\n\tmov.b64 %3, {t6,t7};\n\t"
+      "mov.b64 %4, {t8,t9};\n\tmov.b64 %5, {t10,t11};\n\t"
+      "mov.b64 %6, {t12,t13};\n\tmov.b64 %7, {t14,t15};\n\t"
+      "mov.b64 %8, {t16,t17};\n\tmov.b64 %9, {t18,t19};\n\t"
+      "mov.b64 %10, {t20,t21};\n\tmov.b64 %11, {t22,t23};\n\t"
+      "mov.b64 %12, {t24,t25};\n\tmov.b64 %13, {t26,t27};\n\t"
+      "mov.b64 %14, {t28,t29};\n\tmov.b64 %15, {t30,t31};\n\t}\n"
+      : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]),
+        "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]),
+        "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// acc = v * s + acc on a pair of fp32 lanes (packed f32x2 fused multiply-add).
+__device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t v, uint64_t s2) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(v), "l"(s2));
+}
+
+__device__ __forceinline__ uint64_t splat2(float s) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(s));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 f;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+  return f;
+}
+
+// 4-byte asynchronous global -> shared copy (no register round trip).
+__device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src)
+               : "memory");
+}
+
+// Arrive on *bar once every cp.async this thread issued so far has landed;
+// the arrival counts against the barrier's expected count (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Register reconfiguration of a whole warpgroup (all 128 threads execute it).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -34,17 +34,34 @@ constexpr int kBM = 128;  // rows of A per tile (UMMA M)
 constexpr int kBK = 128;  // K per stage = one scale block
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
 
+// BN = 256: three warpgroups.  Warpgroup 0 (warps 0-3) holds the TMA
+// producer (warp 0) and the MMA issuer (warp 1) and gives registers away
+// (setmaxnreg 24); warpgroups 1-2 (warps 4-11) are the eight epilogue warps
+// (setmaxnreg 240).  128*24 + 256*240 = 64512 = 384 threads * 168 registers,
+// the allocation the kernel is launched with (checked on the host).
+// Warp 2 streams the scales into shared memory.  BN = 128: seven warps, two
+// per sub-partition at most, no reconfiguration.
 template <int BN>
 struct GemmCfg {
   static constexpr int kStages = (BN == 256) ? 4 : 6;
   static constexpr int kEpiWarps = BN / 32;  // 128 columns per warp
-  static constexpr int kThreads = 64 + kEpiWarps * 32;
+  static constexpr int kEpiWarp0 = (BN == 256) ? 4 : 3;
+  static constexpr int kScaleWarp = 2;       // streams the scales into smem
+  static constexpr int kScaleSlots = 8;      // K blocks of scales in flight
+  static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+  static constexpr bool kRegSplit = (BN == 256);
+  static constexpr int kLaunchRegs = 168;
+  static constexpr int kProducerRegs = 24;
+  static constexpr int kEpilogueRegs = 240;
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kBarrierBytes = 256;
-  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kBarrierBytes + 1024;
+  // scale ring: [slot][128] activation scales (raw bits) + [slot][2] weight scales
+  static constexpr int kScaleBytes = kScaleSlots * (kBM + 2) * 4;
+  static constexpr int kBarrierBytes = 512;
+  static constexpr size_t kSmemBytes =
+      (size_t)kStages * kStageBytes + kScaleBytes + kBarrierBytes + 1024;
 };
 
 struct GemmParams {
@@ -65,15 +82,6 @@ struct GemmParams {
   int a_fmt;
 };
 
-__device__ __forceinline__ float act_scale(const GemmParams& p, const void* sa, int kb, int m) {
-  if (p.a_fmt == BFQ_SCALE_UE8M0_PACKED) {
-    const uint32_t w = __ldg((const uint32_t*)sa + (int64_t)(kb >> 2) * p.sa_ld + m);
-    const uint32_t b = (w >> (8 * (kb & 3))) & 0xFFu;
-    return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);  // 2^(b-127)
-  }
-  return __ldg((const float*)sa + (int64_t)kb * p.sa_ld + m);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -88,11 +96,15 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::kStages * C::kABytes;
-  uint64_t* full = (uint64_t*)(smem + (size_t)C::kStages * C::kStageBytes);
+  uint32_t* sc_a = (uint32_t*)(smem + (size_t)C::kStages * C::kStageBytes);  // [slot][128]
+  uint32_t* sc_w = sc_a + C::kScaleSlots * kBM;                                 // [slot][2]
+  uint64_t* full = (uint64_t*)(smem + (size_t)C::kStages * C::kStageBytes + C::kScaleBytes);
   uint64_t* empty = full + C::kStages;
   uint64_t* tfull = empty + C::kStages;
   uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* sfull = tempty + 2;
+  uint64_t* sempty = sfull + C::kScaleSlots;
+  uint64_t* drain = sempty + C::kScaleSlots;
   uint32_t* tmem_slot = (uint32_t*)(drain + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
@@ -128,6 +140,10 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], C::kEpiWarps);
     }
+    for (int b = 0; b < C::kScaleSlots; ++b) {
+      mbar_init(&sfull[b], 32);
+      mbar_init(&sempty[b], C::kEpiWarps);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     *last_flag = 0;
@@ -143,67 +159,101 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  static_assert(!C::kRegSplit || 128 * C::kProducerRegs + 256 * C::kEpilogueRegs <=
+                                     C::kThreads * C::kLaunchRegs,
+                "register split exceeds the launch allocation");
 
-  if (warp == 0) {
-    // ------------------------------ TMA producer ------------------------------
-    if (lane == 0) {
-      const int a_row = (MASKED ? e * p.M : 0) + m0;
-      const int w_row = (MASKED ? e * p.N : 0) + n0;
-      int issued = 0;
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % C::kStages;
-        const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)C::kStageBytes);
-        const int kx = (kb_begin + i) * kBK;
-        tma_load_2d_nohint(sA + (size_t)s * C::kABytes, &tmA, &full[s], kx, a_row);
-        tma_load_2d_nohint(sB + (size_t)s * C::kBBytes, &tmW, &full[s], kx, w_row);
-        ++issued;
-      }
-      if (*abort_flag) {
-        // let the copies already issued land before the CTA can exit
-        for (int j = issued - C::kStages < 0 ? 0 : issued - C::kStages; j < issued; ++j) {
-          volatile int no_abort = 0;
-          (void)mbar_wait(&full[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, &no_abort,
-                          p.status, kWaitTimeoutNs / 8);
+  if (warp < C::kEpiWarp0) {
+    if (C::kRegSplit) setmaxnreg_dec<C::kProducerRegs>();
+    if (warp == 0) {
+      // ------------------------------ TMA producer ------------------------------
+      if (lane == 0) {
+        const int a_row = (MASKED ? e * p.M : 0) + m0;
+        const int w_row = (MASKED ? e * p.N : 0) + n0;
+        int issued = 0;
+        for (int i = 0; i < nk; ++i) {
+          const int s = i % C::kStages;
+          const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)C::kStageBytes);
+          const int kx = (kb_begin + i) * kBK;
+          tma_load_2d_nohint(sA + (size_t)s * C::kABytes, &tmA, &full[s], kx, a_row);
+          tma_load_2d_nohint(sB + (size_t)s * C::kBBytes, &tmW, &full[s], kx, w_row);
+          ++issued;
+        }
+        if (*abort_flag) {
+          // let the copies already issued land before the CTA can exit
+          for (int j = issued - C::kStages < 0 ? 0 : issued - C::kStages; j < issued; ++j) {
+            volatile int no_abort = 0;
+            (void)mbar_wait(&full[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, &no_abort,
+                            p.status, kWaitTimeoutNs / 8);
+          }
         }
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------- MMA issuer -------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
-      bool issued_any = false;
+    } else if (warp == 1) {
+      // ------------------------------- MMA issuer -------------------------------
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+        bool issued_any = false;
+        for (int i = 0; i < nk; ++i) {
+          const int s = i % C::kStages;
+          const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+          const int buf = i & 1;
+          const uint32_t tph = (uint32_t)(i >> 1) & 1u;
+          if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
+          tc_fence_after_sync();
+          if (!mbar_wait(&full[s], ph, abort_flag, p.status, kWaitTimeoutNs)) break;
+          tc_fence_after_sync();
+          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + (size_t)s * C::kABytes));
+          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + (size_t)s * C::kBBytes));
+          const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+  #pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            umma_e4m3(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                      kk > 0 ? 1u : 0u);
+          umma_commit(&empty[s]);
+          umma_commit(&tfull[buf]);
+          issued_any = true;
+        }
+        if (*abort_flag && issued_any) {
+          // wait for the MMAs already issued before TMEM is released
+          umma_commit(drain);
+          volatile int no_abort = 0;
+          (void)mbar_wait(drain, 0, &no_abort, p.status, kWaitTimeoutNs / 8);
+        }
+      }
+    } else if (warp == C::kScaleWarp) {
+      // ------------------------------ scale loader ------------------------------
+      // Per K block: raw bits of sA for the tile's 128 rows (fp32 bits, or the
+      // packed word that holds this block's exponent) and sW for its 1-2 weight
+      // row-blocks, copied asynchronously into a ring slot.  Rows past the valid
+      // range are not copied (their outputs are never stored).
+      const int KBs = KB;
+      const int nb0 = n0 / 128;
+      const int nblks = (int)((p.N + 127) / 128);
+      const void* sa = MASKED ? (const void*)((const char*)p.sa + (int64_t)e * p.sa_estride * 4)
+                              : p.sa;
+      const float* sw = p.sw + (MASKED ? (int64_t)e * p.sw_estride : 0);
+      const bool packed = p.a_fmt == BFQ_SCALE_UE8M0_PACKED;
       for (int i = 0; i < nk; ++i) {
-        const int s = i % C::kStages;
-        const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
-        const int buf = i & 1;
-        const uint32_t tph = (uint32_t)(i >> 1) & 1u;
-        if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
-        tc_fence_after_sync();
-        if (!mbar_wait(&full[s], ph, abort_flag, p.status, kWaitTimeoutNs)) break;
-        tc_fence_after_sync();
-        const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + (size_t)s * C::kABytes));
-        const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + (size_t)s * C::kBBytes));
-        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
-#pragma unroll
-        for (int kk = 0; kk < kBK / 32; ++kk)
-          umma_e4m3(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
-                    kk > 0 ? 1u : 0u);
-        umma_commit(&empty[s]);
-        umma_commit(&tfull[buf]);
-        issued_any = true;
+        const int slot = i % C::kScaleSlots;
+        const uint32_t ph = (uint32_t)(i / C::kScaleSlots) & 1u;
+        if (!mbar_wait(&sempty[slot], ph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
+        const int kb = kb_begin + i;
+        const uint32_t* col = (const uint32_t*)sa + (int64_t)(packed ? (kb >> 2) : kb) * p.sa_ld;
+  #pragma unroll
+        for (int r = lane; r < kBM; r += 32)
+          if (m0 + r < m_limit) cp_async_4(&sc_a[slot * kBM + r], col + m0 + r);
+        if (lane < BN / 128 && nb0 + lane < nblks)
+          cp_async_4(&sc_w[slot * 2 + lane], sw + (int64_t)(nb0 + lane) * KBs + kb);
+        cp_async_arrive_noinc(&sfull[slot]);
       }
-      if (*abort_flag && issued_any) {
-        // wait for the MMAs already issued before TMEM is released
-        umma_commit(drain);
-        volatile int no_abort = 0;
-        (void)mbar_wait(drain, 0, &no_abort, p.status, kWaitTimeoutNs / 8);
-      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
     }
   } else {
+    if (C::kRegSplit) setmaxnreg_inc<C::kEpilogueRegs>();
     // ------------------------- epilogue / promotion ---------------------------
-    const int ew = warp - 2;
+    const int ew = warp - C::kEpiWarp0;
     const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
     const int half = (BN == 256) ? (ew >> 2) : 0;
     const int row_local = quarter * 32 + lane;
@@ -212,22 +262,29 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
     const int col0 = n0 + half * 128;
     const bool warp_active = (m0 + quarter * 32 < m_limit) && (col0 < p.N);
     const int ncols = min(128, p.N - col0);  // multiple of 64 when positive
-    const int nblk = col0 / 128;
-    const float* sw = p.sw + (MASKED ? (int64_t)e * p.sw_estride : 0) + (int64_t)nblk * KB;
-    const void* sa = MASKED ? (const void*)((const char*)p.sa +
-                                            (int64_t)e * p.sa_estride * 4)
-                            : p.sa;
 
-    float acc[128];
+    uint64_t acc[64];  // 128 fp32 accumulators as pairs (column 2i low)
 #pragma unroll
-    for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+    for (int j = 0; j < 64; ++j) acc[j] = 0ull;
 
     for (int i = 0; i < nk; ++i) {
       const int buf = i & 1;
       const uint32_t tph = (uint32_t)(i >> 1) & 1u;
-      const int kb = kb_begin + i;
-      float sc = 0.0f;
-      if (warp_active) sc = (row_ok ? act_scale(p, sa, kb, m) : 0.0f) * __ldg(sw + kb);
+      const int slot = i % C::kScaleSlots;
+      const uint32_t sph = (uint32_t)(i / C::kScaleSlots) & 1u;
+      if (!mbar_wait(&sfull[slot], sph, abort_flag, p.status, kWaitTimeoutNs)) break;
+      const uint32_t a_bits = sc_a[slot * kBM + row_local];
+      const float w_s = __uint_as_float(sc_w[slot * 2 + half]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[slot]);
+      float sa_v;
+      if (p.a_fmt == BFQ_SCALE_UE8M0_PACKED) {
+        const uint32_t b = (a_bits >> (8 * ((kb_begin + i) & 3))) & 0xFFu;
+        sa_v = b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);  // 2^(b-127)
+      } else {
+        sa_v = __uint_as_float(a_bits);
+      }
+      const uint64_t s2 = splat2(__fmul_rn(row_ok ? sa_v : 0.0f, w_s));
       if (!mbar_wait(&tfull[buf], tph, abort_flag, p.status, kWaitTimeoutNs)) break;
       tc_fence_after_sync();
       if (warp_active) {
@@ -235,10 +292,10 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
                                (uint32_t)(buf * BN + half * 128);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32_wait(taddr + (uint32_t)(c * 32), v);
+          uint64_t v[16];
+          tmem_ld32_pairs_wait(taddr + (uint32_t)(c * 32), v);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = __fmaf_rn(v[j], sc, acc[c * 32 + j]);
+          for (int t = 0; t < 16; ++t) ffma2(acc[c * 16 + t], v[t], s2);
         }
       }
       tc_fence_before_sync();
@@ -253,11 +310,12 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
         __nv_bfloat16* dst = p.out + out_row + col0;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          if (c * 8 < ncols)
-            st_v4(dst + c * 8, make_uint4(pack_bf16x2(acc[c * 8 + 0], acc[c * 8 + 1]),
-                                          pack_bf16x2(acc[c * 8 + 2], acc[c * 8 + 3]),
-                                          pack_bf16x2(acc[c * 8 + 4], acc[c * 8 + 5]),
-                                          pack_bf16x2(acc[c * 8 + 6], acc[c * 8 + 7])));
+          if (c * 8 < ncols) {
+            const float2 f0 = unpack2(acc[c * 4 + 0]), f1 = unpack2(acc[c * 4 + 1]);
+            const float2 f2 = unpack2(acc[c * 4 + 2]), f3 = unpack2(acc[c * 4 + 3]);
+            st_v4(dst + c * 8, make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
+                                          pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
+          }
         }
       }
     } else {
@@ -266,13 +324,14 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
         float* part = p.ws + ((int64_t)split * p.M + m) * p.N + col0;
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          if (c * 4 < ncols)
-            *reinterpret_cast<float4*>(part + c * 4) =
-                make_float4(acc[c * 4], acc[c * 4 + 1], acc[c * 4 + 2], acc[c * 4 + 3]);
+          if (c * 4 < ncols) {
+            const float2 f0 = unpack2(acc[c * 2]), f1 = unpack2(acc[c * 2 + 1]);
+            *reinterpret_cast<float4*>(part + c * 4) = make_float4(f0.x, f0.y, f1.x, f1.y);
+          }
       }
       __threadfence();
       named_barrier(1, C::kEpiWarps * 32);
-      if (threadIdx.x == 64) {
+      if (threadIdx.x == C::kEpiWarp0 * 32) {
         const int old = atomicAdd(p.counters + tile, 1);
         const int last = (old == p.splits - 1);
         if (last) p.counters[tile] = 0;  // leave the workspace ready for the next call
@@ -399,6 +458,16 @@ bfq_status launch(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMa
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!configured[dev.ordinal]) {
+      if (C::kRegSplit) {
+        // setmaxnreg.inc only completes if the launch allocation covers the
+        // split; refuse to launch a build whose register count differs.
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, gemm_block_fp8_kernel<BN, MASKED>) != cudaSuccess) {
+          cudaGetLastError();
+          return BFQ_ERR_CUDA;
+        }
+        if (fa.numRegs != C::kLaunchRegs) return BFQ_ERR_DEVICE;
+      }
       if (cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)C::kSmemBytes) != cudaSuccess) {
