@@ -70,6 +70,8 @@ def load_library(build: bool = True):
             "bfq_gemm_block_fp8": (I32, [P, P, I32, I64, P, P, I64, I64, I64, P, P, SZ, P]),
             "bfq_gemm_block_fp8_masked": (I32, [P, P, I32, I64, P, P, P, I32, I32, I64, I64,
                                                 I32, P, P, SZ, P]),
+            "bfq_gemm_block_fp8_noalloc": (I32, [P, P, I32, I64, P, P, I64, I64, I64, P, P]),
+            "bfq_gemm_noalloc_scratch_bytes": (SZ, []),
             "bfq_poll_device_status": (I32, [P]),
             "bfq_watchdog_selftest": (I32, [I32, P]),
         }
@@ -155,6 +157,19 @@ def bfq_gemm_block_fp8(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w_scales
            lib.bfq_gemm_block_fp8(_ptr(a_q), _ptr(a_scales), a_fmt, a_scale_ld, _ptr(w_q),
                                   _ptr(w_scales), M, N, K, _ptr(out), _ptr(workspace), ws_bytes,
                                   _stream(stream)))
+
+
+def bfq_gemm_block_fp8_noalloc(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w_scales, out,
+                               stream=None) -> None:
+    """bfq_gemm_block_fp8 without a workspace argument: for callers that may not
+    allocate device memory (see include/bfq.h).  Calls must not overlap on the GPU."""
+    lib = load_library()
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    _check("bfq_gemm_block_fp8_noalloc",
+           lib.bfq_gemm_block_fp8_noalloc(_ptr(a_q), _ptr(a_scales), a_fmt, a_scale_ld,
+                                          _ptr(w_q), _ptr(w_scales), M, N, K, _ptr(out),
+                                          _stream(stream)))
 
 
 def bfq_gemm_block_fp8_masked(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w_scales,

@@ -600,3 +600,74 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked(
   return bn == 256 ? launch<256, true>(dev, ma, mw, p, (unsigned)grid, s)
                    : launch<128, true>(dev, ma, mw, p, (unsigned)grid, s);
 }
+
+// ----------------------------------------------------------------------------
+// Entry point that allocates nothing.
+//
+// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is
+// captured in global mode (allocation is an error there), plugins inside a
+// host framework that owns every byte of device memory, and serving loops
+// that forbid allocation after start-up because cudaMalloc can synchronize
+// the device.  For them the split-K scratch lives in this file-scope device
+// array, which every GPU that loads the library holds until the process
+// exits.  In host code the array's name is only a host-side stand-in; its
+// device address is looked up with cudaGetSymbolAddress, once per device,
+// with that device current.
+// ----------------------------------------------------------------------------
+namespace bfq {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* g_noalloc_ptr[64];
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device (set-up on the
+// first call per device).  Returns BFQ_OK or BFQ_ERR_CUDA.
+bfq_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return BFQ_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return BFQ_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return BFQ_OK;
+}
+
+}  // namespace
+}  // namespace bfq
+
+extern "C" size_t bfq_gemm_noalloc_scratch_bytes(void) { return bfq::kNoAllocScratchBytes; }
+
+extern "C" bfq_status bfq_gemm_block_fp8_noalloc(const void* a_q, const void* a_scales,
+                                                 int32_t a_fmt, int64_t a_scale_ld,
+                                                 const void* w_q, const float* w_scales,
+                                                 int64_t M, int64_t N, int64_t K, void* out,
+                                                 void* stream) {
+  // The plan's scratch must fit the static array; larger plans are refused.
+  const size_t need = bfq_gemm_workspace_bytes(M, N, K);
+  if (need > bfq::kNoAllocScratchBytes) return BFQ_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (need > 0) {
+    bfq_status st = bfq::noalloc_scratch(&scratch);
+    if (st != BFQ_OK) return st;
+    // The array keeps whatever the previous call left; the tile counters at
+    // its start must begin at zero.
+    if (cudaMemsetAsync(scratch, 0, bfq::kCounterBytes, (cudaStream_t)stream) != cudaSuccess) {
+      cudaGetLastError();
+      return BFQ_ERR_CUDA;
+    }
+  }
+  return bfq_gemm_block_fp8(a_q, a_scales, a_fmt, a_scale_ld, w_q, w_scales, M, N, K, out,
+                            scratch, need > 0 ? bfq::kNoAllocScratchBytes : 0, stream);
+}

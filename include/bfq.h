@@ -194,6 +194,40 @@ bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, int32_t a_f
                               size_t workspace_bytes, void* stream);
 
 /*
+ * bfq_gemm_block_fp8 for callers that cannot allocate device memory.  (The
+ * pages have no counterpart; this is a convenience of this library.)
+ *
+ * Some callers cannot call cudaMalloc: code running while a CUDA graph is
+ * captured in global mode (allocation is an error there), plugins inside a
+ * framework that owns all device memory, and serving loops that forbid
+ * allocation after start-up because cudaMalloc can synchronize the device.
+ * This entry point takes the same arguments as bfq_gemm_block_fp8 minus the
+ * workspace and computes the same result with the same launch plan; its
+ * split-K scratch is a static device array of bfq_gemm_noalloc_scratch_bytes()
+ * (32 MiB) that every GPU loading the library holds until the process exits.
+ *  - It allocates nothing and frees nothing (no cudaMalloc, no library
+ *    allocator); inputs and outputs are still the caller's.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Each call zeroes the array's 4 KiB of tile counters on `stream`
+ *    (cudaMemsetAsync) before the GEMM.
+ *  - All calls share the one array: calls that overlap on the GPU (different
+ *    streams, or concurrent graph launches) race and corrupt each other.
+ *    Serialize them.
+ *  - A problem whose plan needs more scratch than the array holds returns
+ *    BFQ_ERR_WORKSPACE and launches nothing.
+ * Errors: those of bfq_gemm_block_fp8, plus WORKSPACE.
+ */
+bfq_status bfq_gemm_block_fp8_noalloc(const void* a_q, const void* a_scales, int32_t a_fmt,
+                                      int64_t a_scale_ld, const void* w_q,
+                                      const float* w_scales, int64_t M, int64_t N, int64_t K,
+                                      void* out, void* stream);
+
+/* Size in bytes of the static scratch array of bfq_gemm_block_fp8_noalloc. */
+size_t bfq_gemm_noalloc_scratch_bytes(void);
+
+/*
  * Masked grouped block-scaled FP8 GEMM ([PR-19111]
  * m_grouped_gemm_fp8_fp8_bf16_nt_masked; per-expert valid-row count):
  *
