@@ -338,6 +338,58 @@ __device__ __forceinline__ void tmem_ld32_pairs_wait(uint32_t taddr, uint64_t (&
       : "memory");
 }
 
+// 64 consecutive fp32 columns of this warp's 32 TMEM lanes as 32 register
+// pairs (column 2i in the low half of p[i]), load and wait in one statement.
+__device__ __forceinline__ void tmem_ld64_pairs_wait(uint32_t taddr, uint64_t (&p)[32]) {
+  asm volatile(
+      "{\n\t.reg .b32 t<64>;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31,t32,t33,t34,t35,t36,t37,t38,t39,t40,t41,t42,t43,t44,t45,t46,t47,t48,t49,t50,t51,t52,t53,t54,t55,t56,t57,t58,t59,t60,t61,t62,t63}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "mov.b64 %0, {t0,t1};\n\t"
+      "mov.b64 %1, {t2,t3};\n\t"
+      "mov.b64 %2, {t4,t5};\n\t"
+      "mov.b64 %3, {t6,t7};\n\t"
+      "mov.b64 %4, {t8,t9};\n\t"
+      "mov.b64 %5, {t10,t11};\n\t"
+      "mov.b64 %6, {t12,t13};\n\t"
+      "mov.b64 %7, {t14,t15};\n\t"
+      "mov.b64 %8, {t16,t17};\n\t"
+      "mov.b64 %9, {t18,t19};\n\t"
+      "mov.b64 %10, {t20,t21};\n\t"
+      "mov.b64 %11, {t22,t23};\n\t"
+      "mov.b64 %12, {t24,t25};\n\t"
+      "mov.b64 %13, {t26,t27};\n\t"
+      "mov.b64 %14, {t28,t29};\n\t"
+      "mov.b64 %15, {t30,t31};\n\t"
+      "mov.b64 %16, {t32,t33};\n\t"
+      "mov.b64 %17, {t34,t35};\n\t"
+      "mov.b64 %18, {t36,t37};\n\t"
+      "mov.b64 %19, {t38,t39};\n\t"
+      "mov.b64 %20, {t40,t41};\n\t"
+      "mov.b64 %21, {t42,t43};\n\t"
+      "mov.b64 %22, {t44,t45};\n\t"
+      "mov.b64 %23, {t46,t47};\n\t"
+      "mov.b64 %24, {t48,t49};\n\t"
+      "mov.b64 %25, {t50,t51};\n\t"
+      "mov.b64 %26, {t52,t53};\n\t"
+      "mov.b64 %27, {t54,t55};\n\t"
+      "mov.b64 %28, {t56,t57};\n\t"
+      "mov.b64 %29, {t58,t59};\n\t"
+      "mov.b64 %30, {t60,t61};\n\t"
+      "mov.b64 %31, {t62,t63};\n\t"
+      "}\n"
+      : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]), "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23]), "=l"(p[24]), "=l"(p[25]), "=l"(p[26]), "=l"(p[27]), "=l"(p[28]), "=l"(p[29]), "=l"(p[30]), "=l"(p[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Cluster-wide barrier (all threads of all CTAs of the cluster), with
+// release/acquire ordering of the memory operations around it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // acc = v * s + acc on a pair of fp32 lanes (packed f32x2 fused multiply-add).
 __device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t v, uint64_t s2) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(v), "l"(s2));

@@ -33,6 +33,7 @@ namespace bfq {
 constexpr int kBM = 128;  // rows of A per tile (UMMA M)
 constexpr int kBK = 128;  // K per stage = one scale block
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
+constexpr int kMaxSplits = 8;  // K splits of a tile form one (portable-size) cluster
 
 // BN = 256: three warpgroups.  Warpgroup 0 (warps 0-3) holds the TMA
 // producer (warp 0) and the MMA issuer (warp 1) and gives registers away
@@ -73,7 +74,6 @@ struct GemmParams {
   __nv_bfloat16* out;      // [rows][N]
   int64_t out_estride;     // elements of out per expert (masked)
   float* ws;               // split-K partials [splits][M][N]
-  int* counters;           // split-K tile counters [tiles], zero between calls
   const int32_t* counts;   // masked: per-expert valid rows
   int* status;             // device error latch
   int M;                   // dense: rows of A; masked: rows per expert (T)
@@ -107,7 +107,6 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
   uint64_t* drain = sempty + C::kScaleSlots;
   uint32_t* tmem_slot = (uint32_t*)(drain + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-  volatile int* last_flag = abort_flag + 1;
 
   // ---- tile decode: split fastest, then m tile, then n tile, then expert ----
   const int split = blockIdx.x % p.splits;
@@ -146,7 +145,6 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
-    *last_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmW);
@@ -250,6 +248,8 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
     }
+    __syncwarp();
+    if (p.splits > 1) cluster_sync();  // pairs with the epilogue's barrier
   } else {
     if (C::kRegSplit) setmaxnreg_inc<C::kEpilogueRegs>();
     // ------------------------- epilogue / promotion ---------------------------
@@ -291,11 +291,11 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                (uint32_t)(buf * BN + half * 128);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint64_t v[16];
-          tmem_ld32_pairs_wait(taddr + (uint32_t)(c * 32), v);
+        for (int h = 0; h < 2; ++h) {
+          uint64_t v[32];
+          tmem_ld64_pairs_wait(taddr + (uint32_t)(h * 64), v);
 #pragma unroll
-          for (int t = 0; t < 16; ++t) ffma2(acc[c * 16 + t], v[t], s2);
+          for (int t = 0; t < 32; ++t) ffma2(acc[h * 32 + t], v[t], s2);
         }
       }
       tc_fence_before_sync();
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
         }
       }
     } else {
-      // split-K: publish the fp32 partial, the last CTA of the tile reduces.
+      // split-K: publish this split's fp32 partial; the cluster reduces below.
       if (ok && warp_active && row_ok) {
         float* part = p.ws + ((int64_t)split * p.M + m) * p.N + col0;
 #pragma unroll
@@ -329,35 +329,35 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
             *reinterpret_cast<float4*>(part + c * 4) = make_float4(f0.x, f0.y, f1.x, f1.y);
           }
       }
+      // The K splits of one tile are one thread-block cluster.  After every
+      // CTA has published its partial (every thread of the cluster passes one
+      // cluster barrier), CTA `split` reduces the split-th slice of the tile,
+      // summing the partials in split order (deterministic).
       __threadfence();
-      named_barrier(1, C::kEpiWarps * 32);
-      if (threadIdx.x == C::kEpiWarp0 * 32) {
-        const int old = atomicAdd(p.counters + tile, 1);
-        const int last = (old == p.splits - 1);
-        if (last) p.counters[tile] = 0;  // leave the workspace ready for the next call
-        *last_flag = last;
-      }
-      named_barrier(1, C::kEpiWarps * 32);
-      if (*last_flag) {
-        __threadfence();
-        if (ok && warp_active && row_ok) {
-          __nv_bfloat16* dst = p.out + out_row + col0;
-#pragma unroll 1
-          for (int c = 0; c < 16; ++c) {
-            if (c * 8 >= ncols) break;
-            float v[8];
+      cluster_sync();
+      if (!*abort_flag) {
+        const int rows = min(kBM, m_limit - m0);
+        const int upr = min(BN, p.N - n0) / 4;  // float4 units per row
+        const int total = rows * upr;
+        const int u_begin = (int)((int64_t)split * total / p.splits);
+        const int u_end = (int)((int64_t)(split + 1) * total / p.splits);
+        for (int u = u_begin + (int)threadIdx.x - C::kEpiWarp0 * 32; u < u_end;
+             u += C::kEpiWarps * 32) {
+          const int r = u / upr, c4 = u - (u / upr) * upr;
+          const int64_t off = (int64_t)(m0 + r) * p.N + n0 + c4 * 4;
+          float4 v[kMaxSplits];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-            for (int s = 0; s < p.splits; ++s) {
-              const float* src = p.ws + ((int64_t)s * p.M + m) * p.N + col0 + c * 8;
-              const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
-              const float4 b = __ldcg(reinterpret_cast<const float4*>(src + 4));
-              v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
-              v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+          for (int t = 0; t < kMaxSplits; ++t)
+            if (t < p.splits)
+              v[t] = __ldcg(reinterpret_cast<const float4*>(p.ws + (int64_t)t * p.M * p.N + off));
+          float4 a4 = v[0];
+#pragma unroll
+          for (int t = 1; t < kMaxSplits; ++t)
+            if (t < p.splits) {
+              a4.x += v[t].x; a4.y += v[t].y; a4.z += v[t].z; a4.w += v[t].w;
             }
-            st_v4(dst + c * 8, make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                          pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7])));
-          }
+          *reinterpret_cast<uint2*>(p.out + off) =
+              make_uint2(pack_bf16x2(a4.x, a4.y), pack_bf16x2(a4.z, a4.w));
         }
       }
     }
@@ -417,18 +417,16 @@ struct Plan {
   size_t ws_bytes = 0;  // bytes needed by this plan
 };
 
-// Workspace layout of a split-K plan: a fixed 4 KiB block of tile counters
-// at offset 0 (split-K only runs when there are fewer tiles than SMs, so at
-// most 1024 tiles), then the fp32 partial sums [splits][M][N].  The counters
-// always sit at the same place and every call returns the ones it used to
-// zero, so a zero-filled workspace stays valid across calls of any shape.
-constexpr size_t kCounterBytes = 4096;
-constexpr int kMaxSplitTiles = (int)(kCounterBytes / sizeof(int));
-
+// Workspace of a split-K plan: the fp32 partial sums [splits][M][N].  Every
+// element a call reads was written earlier in the same call, so the buffer
+// needs no initialisation and one buffer serves calls of any shape.
 size_t split_ws_bytes(int64_t M, int64_t N, int splits) {
   if (splits <= 1) return 0;
-  return kCounterBytes + (size_t)splits * (size_t)M * (size_t)N * sizeof(float);
+  return (size_t)splits * (size_t)M * (size_t)N * sizeof(float);
 }
+
+template <int BN>
+int max_active_clusters(const DeviceInfo& dev, int cluster);
 
 Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, size_t ws_avail,
                 bool limit_by_ws) {
@@ -439,9 +437,14 @@ Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, size_t w
   const int tiles = pl.m_tiles * pl.n_tiles;
   const int KB = (int)(K / kBK);
   int splits = 1;
-  if (tiles < dev.sm_count && tiles <= kMaxSplitTiles) splits = dev.sm_count / tiles;
+  if (tiles < dev.sm_count) splits = dev.sm_count / tiles;
+  if (splits > kMaxSplits) splits = kMaxSplits;
   if (splits > KB) splits = KB;
   if (splits < 1) splits = 1;
+  // all clusters of the grid should be resident at once
+  while (splits > 1 && (pl.bn == 256 ? max_active_clusters<256>(dev, splits)
+                                     : max_active_clusters<128>(dev, splits)) < tiles)
+    --splits;
   if (limit_by_ws)
     while (splits > 1 && split_ws_bytes(M, N, splits) > ws_avail) --splits;
   pl.splits = splits;
@@ -450,32 +453,87 @@ Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, size_t w
 }
 
 template <int BN, bool MASKED>
-bfq_status launch(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
-                  const GemmParams& p, unsigned grid, cudaStream_t s) {
+bfq_status configure(const DeviceInfo& dev) {
   using C = GemmCfg<BN>;
   static bool configured[64] = {};
   static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (configured[dev.ordinal]) return BFQ_OK;
+  if (C::kRegSplit) {
+    // setmaxnreg.inc only completes if the launch allocation covers the
+    // split; refuse to launch a build whose register count differs.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, gemm_block_fp8_kernel<BN, MASKED>) != cudaSuccess) {
+      cudaGetLastError();
+      return BFQ_ERR_CUDA;
+    }
+    if (fa.numRegs != C::kLaunchRegs) return BFQ_ERR_DEVICE;
+  }
+  if (cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)C::kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return BFQ_ERR_CUDA;
+  }
+  configured[dev.ordinal] = true;
+  return BFQ_OK;
+}
+
+// Clusters of `cluster` CTAs of the dense kernel that fit on the device at
+// once (cached per device and size; 0 when unknown).
+template <int BN>
+int max_active_clusters(const DeviceInfo& dev, int cluster) {
+  using C = GemmCfg<BN>;
+  static int cache[64][kMaxSplits + 1];
+  static std::mutex mu;
+  if (cluster < 1 || cluster > kMaxSplits) return 0;
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (!configured[dev.ordinal]) {
-      if (C::kRegSplit) {
-        // setmaxnreg.inc only completes if the launch allocation covers the
-        // split; refuse to launch a build whose register count differs.
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, gemm_block_fp8_kernel<BN, MASKED>) != cudaSuccess) {
-          cudaGetLastError();
-          return BFQ_ERR_CUDA;
-        }
-        if (fa.numRegs != C::kLaunchRegs) return BFQ_ERR_DEVICE;
-      }
-      if (cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)C::kSmemBytes) != cudaSuccess) {
-        cudaGetLastError();
-        return BFQ_ERR_CUDA;
-      }
-      configured[dev.ordinal] = true;
-    }
+    if (cache[dev.ordinal][cluster]) return cache[dev.ordinal][cluster];
+  }
+  if (configure<BN, false>(dev) != BFQ_OK) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(cluster * dev.sm_count));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_block_fp8_kernel<BN, false>, &cfg) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[dev.ordinal][cluster] = n > 0 ? n : -1;
+  return n;
+}
+
+template <int BN, bool MASKED>
+bfq_status launch(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
+                  const GemmParams& p, unsigned grid, cudaStream_t s) {
+  using C = GemmCfg<BN>;
+  bfq_status st = configure<BN, MASKED>(dev);
+  if (st != BFQ_OK) return st;
+  if (p.splits > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, gemm_block_fp8_kernel<BN, MASKED>, ma, mw, p));
   }
   gemm_block_fp8_kernel<BN, MASKED><<<grid, C::kThreads, C::kSmemBytes, s>>>(ma, mw, p);
   return launch_status(cudaGetLastError());
@@ -539,10 +597,7 @@ extern "C" bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, 
   p.n_tiles = pl.n_tiles;
   p.splits = pl.splits;
   p.a_fmt = a_fmt;
-  if (pl.splits > 1) {
-    p.counters = (int*)workspace;
-    p.ws = (float*)((char*)workspace + kCounterBytes);
-  }
+  if (pl.splits > 1) p.ws = (float*)workspace;
   const unsigned grid = (unsigned)(pl.m_tiles * pl.n_tiles * pl.splits);
   cudaStream_t s = (cudaStream_t)stream;
   return pl.bn == 256 ? launch<256, false>(dev, ma, mw, p, grid, s)
@@ -661,12 +716,6 @@ extern "C" bfq_status bfq_gemm_block_fp8_noalloc(const void* a_q, const void* a_
   if (need > 0) {
     bfq_status st = bfq::noalloc_scratch(&scratch);
     if (st != BFQ_OK) return st;
-    // The array keeps whatever the previous call left; the tile counters at
-    // its start must begin at zero.
-    if (cudaMemsetAsync(scratch, 0, bfq::kCounterBytes, (cudaStream_t)stream) != cudaSuccess) {
-      cudaGetLastError();
-      return BFQ_ERR_CUDA;
-    }
   }
   return bfq_gemm_block_fp8(a_q, a_scales, a_fmt, a_scale_ld, w_q, w_scales, M, N, K, out,
                             scratch, need > 0 ? bfq::kNoAllocScratchBytes : 0, stream);

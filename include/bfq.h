@@ -156,11 +156,10 @@ bfq_status bfq_weight_block_quant(const void* w, int64_t batch, int64_t N, int64
 
 /*
  * Bytes of workspace that bfq_gemm_block_fp8 can use for an (M, N, K) problem
- * on the current device: 0 when the launch plan does not split K, else a
- * 4 KiB block of tile counters followed by fp32 partial sums.  The workspace
- * must be zero-filled once after it is allocated; every call returns the
- * counters it used to zero, so one buffer serves calls of any shape.  Calls
- * that share a workspace must not overlap in time (use one stream).
+ * on the current device: 0 when the launch plan does not split K, else the
+ * fp32 partial sums of the K splits, [splits][M][N].  The buffer needs no
+ * initialisation (each call writes every element it reads) and serves calls
+ * of any shape; calls that share one must not overlap in time.
  */
 size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
@@ -172,7 +171,10 @@ size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *                         * sum_{k in block b} a_q[m, k] * w_q[n, k] )
  *
  * with fp32 accumulation on the tensor cores and the scale product applied
- * to each 128-deep K block ("promotion").
+ * to each 128-deep K block ("promotion").  When there are fewer output tiles
+ * than SMs, K is split over the CTAs of a thread-block cluster (at most 8)
+ * and the partial sums are added in split order, so results are
+ * deterministic.
  *
  *   a_q            e4m3 [M][K], 16-byte aligned.
  *   a_scales       column-major activation scales in format a_fmt
@@ -210,8 +212,6 @@ bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, int32_t a_f
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture.
- *  - Each call zeroes the array's 4 KiB of tile counters on `stream`
- *    (cudaMemsetAsync) before the GEMM.
  *  - All calls share the one array: calls that overlap on the GPU (different
  *    streams, or concurrent graph launches) race and corrupt each other.
  *    Serialize them.

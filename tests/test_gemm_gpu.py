@@ -59,14 +59,14 @@ def test_gemm_split_k_is_deterministic_and_matches_unsplit(cuda_lib, orc):
     assert bfq.bfq_gemm_workspace_bytes(M, N, K) > 0  # this shape is split along K
     aq, sa, wq, sw = _oracle_problem(orc, M, N, K, 0, seed=99)
     d = _to_dev(aq, sa, wq, sw, 0)
-    ws = torch.zeros(bfq.bfq_gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    ws = torch.full((bfq.bfq_gemm_workspace_bytes(M, N, K),), 0x7F, dtype=torch.uint8,
+                    device="cuda")  # garbage: the workspace needs no initialisation
     o1 = bfq.gemm(d[0], d[1], 0, d[2], d[3], workspace=ws)
     o2 = bfq.gemm(d[0], d[1], 0, d[2], d[3], workspace=ws)
     o3 = torch.empty_like(o1)
     bfq.bfq_gemm_block_fp8(d[0], d[1], 0, d[1].shape[-1], d[2], d[3], o3, None)  # unsplit
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
-    assert ws[:4096].count_nonzero().item() == 0  # tile counters back at zero
     ref = orc.gemm(aq, sa, 0, wq, sw)
     an, wn = _norms(orc, aq, sa, wq, sw, 0)
     assert_gemm_close(o1.float().cpu().numpy(), ref, an, wn, "split")
