@@ -125,7 +125,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -305,6 +305,119 @@ def timed_launches(bfq, torch, shapes, reps):
     return qt, gt
 
 
+QUANT_M = [8, 128, 4096, 16384]
+QUANT_K = [7168, 18432]
+MOE_E, MOE_T, MOE_I, MOE_H = 32, 256, 2048, 7168
+
+
+def gated_times(torch, fn, reps):
+    """Per-launch device time (us) of fn(), with the host ahead of the GPU."""
+    ts = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(2_000_000)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    ts.sort()
+    return ts[len(ts) // 2]
+
+
+def measure_quant_sweep(bfq, torch, dev, hbm_peak, reps):
+    """Standalone per-token-group quant over m x k, fp32 and packed UE8M0 scales."""
+    import bfq_synth as synth
+
+    rows = []
+    for k in QUANT_K:
+        for m in QUANT_M:
+            x = synth.activation(m, k, seed=m + k, zero_group=True, device=dev)
+            for fmt, name in ((bfq.SCALE_F32, "f32"), (bfq.SCALE_UE8M0_PACKED, "ue8m0_packed")):
+                ld = bfq.align4(m)
+                q = torch.empty((m, k), dtype=torch.float8_e4m3fn, device=dev)
+                sc = torch.empty((bfq.scale_cols(k, fmt), ld), dtype=bfq.scale_dtype(fmt),
+                                 device=dev)
+                us = gated_times(torch, lambda: bfq.bfq_quant(x, q, sc, fmt, ld), reps)
+                nbytes = 3 * m * k + sc.numel() * 4
+                gbs = nbytes / (us * 1e-6) / 1e9
+                rows.append({"m": m, "k": k, "scales": name, "us": round(us, 2),
+                             "gbps": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 3),
+                             "bytes": nbytes})
+            del x
+    return rows
+
+
+def measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, reps):
+    """Masked MoE expert slice: up GEMM -> silu-mul-quant -> down GEMM, E=32,
+    T_max=256, valid counts ~ U{0..256}, UE8M0 packed activation scales,
+    power-of-two 128x128 weight scales."""
+    import bfq_synth as synth
+
+    E, T, I, H = MOE_E, MOE_T, MOE_I, MOE_H
+    counts = synth.valid_counts(E, T)
+    tot = int(counts.sum())
+    d_counts = counts.to(dev)
+    w_up = torch.empty((E, 2 * I, H), dtype=torch.float8_e4m3fn, device=dev)
+    s_up = torch.empty((E, 2 * I // 128, H // 128), dtype=torch.float32, device=dev)
+    w_dn = torch.empty((E, H, I), dtype=torch.float8_e4m3fn, device=dev)
+    s_dn = torch.empty((E, H // 128, I // 128), dtype=torch.float32, device=dev)
+    for e in range(E):  # one expert at a time keeps the bf16 staging small
+        wq, sw = bfq.weight_block_quant(synth.weight(2 * I, H, seed=700 + e, device=dev),
+                                        bfq.SCALE_F32_POW2)
+        w_up[e].copy_(wq)
+        s_up[e].copy_(sw)
+        wq, sw = bfq.weight_block_quant(synth.weight(H, I, seed=800 + e, device=dev),
+                                        bfq.SCALE_F32_POW2)
+        w_dn[e].copy_(wq)
+        s_dn[e].copy_(sw)
+    x = synth.masked_activation(E, T, H, counts, seed=900, device=dev)
+    a_up = torch.empty((E, T, H), dtype=torch.float8_e4m3fn, device=dev)
+    sa_up = torch.empty((E, bfq.scale_cols(H, 2), T), dtype=torch.int32, device=dev)
+    for e in range(E):
+        c = int(counts[e])
+        if c:
+            bfq.bfq_quant(x[e, :c], a_up[e, :c], sa_up[e], bfq.SCALE_UE8M0_PACKED, T)
+    h = torch.empty((E, T, 2 * I), dtype=torch.bfloat16, device=dev)
+    a_dn = torch.empty((E, T, I), dtype=torch.float8_e4m3fn, device=dev)
+    sa_dn = torch.empty((E, bfq.scale_cols(I, 2), T), dtype=torch.int32, device=dev)
+    out = torch.empty((E, T, H), dtype=torch.bfloat16, device=dev)
+
+    def up():
+        bfq.bfq_gemm_block_fp8_masked(a_up, sa_up, 2, T, w_up, s_up, d_counts, h)
+
+    def act():
+        bfq.bfq_silu_mul_quant(h, d_counts, a_dn, sa_dn, 2, T)
+
+    def down():
+        bfq.bfq_gemm_block_fp8_masked(a_dn, sa_dn, 2, T, w_dn, s_dn, d_counts, out)
+
+    for fn in (up, act, down):
+        fn()
+    torch.cuda.synchronize()
+    active = int((counts > 0).sum())
+    res = {"experts": E, "t_max": T, "valid_rows": tot, "active_experts": active}
+    for name, fn, n, k in (("up_gemm", up, 2 * I, H), ("down_gemm", down, H, I)):
+        us = gated_times(torch, fn, reps)
+        flops = 2.0 * tot * n * k
+        nbytes = active * n * k + tot * k + 2 * tot * n + active * (n // 128) * (k // 128) * 4 \
+            + tot * (k // 512) * 4
+        t_roof = max(flops / (fp8_peak * 1e12), nbytes / (hbm_peak * 1e9))
+        res[name] = {"n": n, "k": k, "us": round(us, 2), "tflops": round(flops / us / 1e6, 1),
+                     "gbps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "roofline_frac": round(t_roof * 1e6 / us, 3),
+                     "bound": "tensor" if flops / (fp8_peak * 1e12) > nbytes / (hbm_peak * 1e9)
+                     else "hbm"}
+    us = gated_times(torch, act, reps)
+    nbytes = tot * (2 * I * 2 + I) + tot * (I // 512) * 4
+    gbs = nbytes / (us * 1e-6) / 1e9
+    res["silu_mul_quant"] = {"us": round(us, 2), "gbps": round(gbs, 1),
+                             "hbm_frac": round(gbs / hbm_peak, 3), "bytes": nbytes}
+    del w_up, w_dn, x, h
+    return res
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
 
@@ -317,6 +430,9 @@ def run_gpu(args, rank, world, local_rank):
     hbm_peak = float(peaks["hbm_gbs"])
     fp8_peak = float(peaks["bf16_tflops"]) * FP8_PER_BF16
 
+    if args.moe_only:  # profiling mode: the MoE expert slice only, no report
+        measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, 2)
+        return 0
     shapes = build_problem(bfq, torch, dev, args.shape)
     n_shapes = len(shapes)
     flops_step = sum(2 * s["m"] * s["n"] * s["k"] for s in shapes)
@@ -460,6 +576,13 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk.summary(),
         "shapes": per_shape,
     }
+    if not args.skip_extra:
+        del shapes
+        torch.cuda.empty_cache()
+        line["quant_sweep"] = measure_quant_sweep(bfq, torch, dev, hbm_peak, 10)
+        line["moe_slice"] = measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, 10)
+        if bfq.bfq_poll_device_status() != 0:
+            raise RuntimeError("device watchdog fired during the extra measurements")
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)
@@ -469,13 +592,17 @@ def run_gpu(args, rank, world, local_rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--shape", type=lambda v: tuple(int(t) for t in v.split(",")), default=None,
                     help="m,n,k of one sweep shape: run only it, eagerly, and print nothing "
                          "(for profiler captures)")
     ap.add_argument("--impl", choices=["bfq", "reference"], default="bfq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--moe-only", action="store_true",
+                    help="run only the masked MoE expert slice and print nothing (profiling)")
+    ap.add_argument("--skip-extra", action="store_true",
+                    help="skip the standalone-quant sweep and the MoE slice measurements")
     args = ap.parse_args(argv)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

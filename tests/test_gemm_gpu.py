@@ -124,3 +124,20 @@ def test_gemm_full_size_sweep_sampled(cuda_lib, orc, N, K):
         got = out.float().cpu().numpy()[rows]
         assert_gemm_close(got, ref, an, wn, f"sweep m={M} n={N} k={K}")
         assert calc_diff(got, ref) < 1e-4
+
+
+@pytest.mark.parametrize("fmt", [0, 2])
+@pytest.mark.parametrize("M,N,K", [(1152, 4096, 384), (2048, 2560, 512)])
+def test_gemm_parity_unsplit_many_tiles(cuda_lib, orc, fmt, M, N, K):
+    """Enough tiles that K is not split (one CTA per output tile), with a
+    ragged and an odd number of m tiles."""
+    bfq = cuda_lib
+    assert bfq.bfq_gemm_workspace_bytes(M, N, K) == 0
+    aq, sa, wq, sw = _oracle_problem(orc, M, N, K, fmt, seed=M + N + K + fmt)
+    d = _to_dev(aq, sa, wq, sw, fmt)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bfq.gemm(d[0], d[1], fmt, d[2], d[3], out=out)
+    torch.cuda.synchronize()
+    ref = orc.gemm(aq, sa, fmt, wq, sw)
+    an, wn = _norms(orc, aq, sa, wq, sw, fmt)
+    assert_gemm_close(out.float().cpu().numpy(), ref, an, wn, f"unsplit {M}x{N}x{K}")
