@@ -90,7 +90,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int BN, bool MASKED>
 __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
     gemm_block_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
-                          const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
+                          const __grid_constant__ CUtensorMap tmW,
+                          const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   using C = GemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
   const int m0 = mt * kBM, n0 = nt * BN;
   int m_limit = p.M;
   if (MASKED) {
+    griddep_wait();  // the counts may come from the previous kernel
     int c = __ldg(p.counts + e);
     m_limit = c < 0 ? 0 : (c > p.M ? p.M : c);
     if (m0 >= m_limit) return;  // whole tile is padding: no loads, no MMA
@@ -157,6 +159,10 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // The set-up above overlaps the previous kernel's tail; nothing below may
+  // touch global memory before that kernel has finished.
+  if (!MASKED) griddep_wait();
+  griddep_launch_dependents();
   static_assert(!C::kRegSplit || 128 * C::kProducerRegs + 256 * C::kEpilogueRegs <=
                                      C::kThreads * C::kLaunchRegs,
                 "register split exceeds the launch allocation");
@@ -305,7 +311,37 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
 
     const bool ok = !*abort_flag;
     const int64_t out_row = (MASKED ? (int64_t)e * p.out_estride : 0) + (int64_t)m * p.N;
-    if (p.splits == 1) {
+    if (p.splits == 1 && !MASKED) {
+      // Dense tile: stage the bf16 tile in the (now idle) A stages as
+      // [BN/64] boxes of 128 rows x 64 columns in the 128-byte swizzled layout
+      // (16-byte chunk c of row r at chunk c ^ (r mod 8): conflict-free), then
+      // one thread writes them with TMA stores, which clip rows >= M.
+      if (ok && warp_active) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int blk = half * 2 + j;
+          if (j * 64 >= ncols) break;  // this 64-column block lies beyond N
+          const uint32_t row_addr =
+              smem_u32(smem) + (uint32_t)(blk * (kBM * 128) + row_local * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int a = j * 32 + c * 4;  // pair index of column j*64 + c*8
+            const float2 f0 = unpack2(acc[a + 0]), f1 = unpack2(acc[a + 1]);
+            const float2 f2 = unpack2(acc[a + 2]), f3 = unpack2(acc[a + 3]);
+            st_shared_v4(row_addr + (uint32_t)((c ^ (row_local & 7)) << 4),
+                         make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
+                                    pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      named_barrier(1, C::kEpiWarps * 32);
+      if (threadIdx.x == C::kEpiWarp0 * 32 && !*abort_flag) {
+        for (int blk = 0; blk < BN / 64; ++blk)
+          if (n0 + blk * 64 < p.N) tma_store_2d(&tmO, smem + blk * (kBM * 128), n0 + blk * 64, m0);
+        bulk_commit_and_wait_all();
+      }
+    } else if (p.splits == 1) {
       if (ok && warp_active && row_ok) {
         __nv_bfloat16* dst = p.out + out_row + col0;
 #pragma unroll
@@ -408,6 +444,21 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2D map over the bf16 output [rows][cols] with a 64 x 128 box and 128-byte
+// swizzling, for TMA stores of the staged tile.
+bool make_out_map(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -516,27 +567,13 @@ int max_active_clusters(const DeviceInfo& dev, int cluster) {
 
 template <int BN, bool MASKED>
 bfq_status launch(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
-                  const GemmParams& p, unsigned grid, cudaStream_t s) {
+                  const CUtensorMap& mo, const GemmParams& p, unsigned grid, cudaStream_t s) {
   using C = GemmCfg<BN>;
   bfq_status st = configure<BN, MASKED>(dev);
   if (st != BFQ_OK) return st;
-  if (p.splits > 1) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(C::kThreads);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return launch_status(cudaLaunchKernelEx(&cfg, gemm_block_fp8_kernel<BN, MASKED>, ma, mw, p));
-  }
-  gemm_block_fp8_kernel<BN, MASKED><<<grid, C::kThreads, C::kSmemBytes, s>>>(ma, mw, p);
-  return launch_status(cudaGetLastError());
+  return launch_status(launch_pdl(gemm_block_fp8_kernel<BN, MASKED>, dim3(grid),
+                                  dim3(C::kThreads), C::kSmemBytes, s,
+                                  p.splits > 1 ? (unsigned)p.splits : 1u, ma, mw, mo, p));
 }
 
 bfq_status check_device(DeviceInfo* dev) {
@@ -579,9 +616,10 @@ extern "C" bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, 
   bfq_status st = check_device(&dev);
   if (st != BFQ_OK) return st;
   Plan pl = dense_plan(dev, M, N, K, workspace ? workspace_bytes : 0, true);
-  CUtensorMap ma, mw;
+  CUtensorMap ma, mw, mo;
   if (!make_map(&ma, a_q, (uint64_t)K, (uint64_t)M, kBM) ||
-      !make_map(&mw, w_q, (uint64_t)K, (uint64_t)N, (uint32_t)pl.bn))
+      !make_map(&mw, w_q, (uint64_t)K, (uint64_t)N, (uint32_t)pl.bn) ||
+      !make_out_map(&mo, out, (uint64_t)N, (uint64_t)M))
     return BFQ_ERR_CUDA;
   GemmParams p{};
   p.sa = a_scales;
@@ -600,8 +638,8 @@ extern "C" bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, 
   if (pl.splits > 1) p.ws = (float*)workspace;
   const unsigned grid = (unsigned)(pl.m_tiles * pl.n_tiles * pl.splits);
   cudaStream_t s = (cudaStream_t)stream;
-  return pl.bn == 256 ? launch<256, false>(dev, ma, mw, p, grid, s)
-                      : launch<128, false>(dev, ma, mw, p, grid, s);
+  return pl.bn == 256 ? launch<256, false>(dev, ma, mw, mo, p, grid, s)
+                      : launch<128, false>(dev, ma, mw, mo, p, grid, s);
 }
 
 extern "C" bfq_status bfq_gemm_block_fp8_masked(
@@ -652,8 +690,8 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked(
   const int64_t grid = (int64_t)p.m_tiles * p.n_tiles * E;
   if (grid > 0x7FFFFFFF) return BFQ_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;
-  return bn == 256 ? launch<256, true>(dev, ma, mw, p, (unsigned)grid, s)
-                   : launch<128, true>(dev, ma, mw, p, (unsigned)grid, s);
+  return bn == 256 ? launch<256, true>(dev, ma, mw, mw, p, (unsigned)grid, s)
+                   : launch<128, true>(dev, ma, mw, mw, p, (unsigned)grid, s);
 }
 
 // ----------------------------------------------------------------------------

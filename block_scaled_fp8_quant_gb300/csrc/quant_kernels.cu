@@ -90,6 +90,8 @@ template <int FMT>
 __global__ void __launch_bounds__(kQuantWarps * 32)
     quant_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K, int64_t ld_x,
                  uint8_t* __restrict__ q, void* __restrict__ scales, int64_t scale_ld) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t G = K / 128;
   const int64_t chunks = (G + 3) / 4;
@@ -140,6 +142,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int I,
                           const int32_t* __restrict__ counts, uint8_t* __restrict__ q,
                           void* __restrict__ scales, int64_t scale_ld) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int e = blockIdx.y;
   int cnt = __ldg(counts + e);
   cnt = cnt < 0 ? 0 : (cnt > T ? T : cnt);
@@ -203,6 +207,8 @@ __global__ void __launch_bounds__(256)
     weight_quant_kernel(const __nv_bfloat16* __restrict__ w, int64_t N, int64_t K,
                         uint8_t* __restrict__ wq, float* __restrict__ sw) {
   __shared__ float red[8];
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t NB = (N + 127) / 128, KB = K / 128;
   const int64_t nb = blockIdx.y, kb = blockIdx.x, b = blockIdx.z;
   const int t = threadIdx.x;
@@ -280,19 +286,22 @@ extern "C" bfq_status bfq_quant(const void* x, int64_t M, int64_t K, int64_t ld_
   auto* qb = (uint8_t*)q;
   switch (fmt) {
     case BFQ_SCALE_F32:
-      quant_kernel<BFQ_SCALE_F32><<<(unsigned)blocks, kQuantWarps * 32, 0, s>>>(
-          xb, M, K, ld_x, qb, scales, scale_ld);
+      st = launch_status(launch_pdl(quant_kernel<BFQ_SCALE_F32>, dim3((unsigned)blocks),
+                                    dim3(kQuantWarps * 32), 0, s, 1, xb, M, K, ld_x, qb, scales,
+                                    scale_ld));
       break;
     case BFQ_SCALE_F32_POW2:
-      quant_kernel<BFQ_SCALE_F32_POW2><<<(unsigned)blocks, kQuantWarps * 32, 0, s>>>(
-          xb, M, K, ld_x, qb, scales, scale_ld);
+      st = launch_status(launch_pdl(quant_kernel<BFQ_SCALE_F32_POW2>, dim3((unsigned)blocks),
+                                    dim3(kQuantWarps * 32), 0, s, 1, xb, M, K, ld_x, qb, scales,
+                                    scale_ld));
       break;
     default:
-      quant_kernel<BFQ_SCALE_UE8M0_PACKED><<<(unsigned)blocks, kQuantWarps * 32, 0, s>>>(
-          xb, M, K, ld_x, qb, scales, scale_ld);
+      st = launch_status(launch_pdl(quant_kernel<BFQ_SCALE_UE8M0_PACKED>, dim3((unsigned)blocks),
+                                    dim3(kQuantWarps * 32), 0, s, 1, xb, M, K, ld_x, qb, scales,
+                                    scale_ld));
       break;
   }
-  return launch_status(cudaGetLastError());
+  return st;
 }
 
 extern "C" bfq_status bfq_silu_mul_quant(const void* x, int32_t E, int32_t T, int32_t I,
@@ -313,19 +322,22 @@ extern "C" bfq_status bfq_silu_mul_quant(const void* x, int32_t E, int32_t T, in
   auto* qb = (uint8_t*)q;
   switch (fmt) {
     case BFQ_SCALE_F32:
-      silu_mul_quant_kernel<BFQ_SCALE_F32><<<grid, kQuantWarps * 32, 0, s>>>(
-          xb, T, I, valid_counts, qb, scales, scale_ld);
+      st = launch_status(launch_pdl(silu_mul_quant_kernel<BFQ_SCALE_F32>, grid,
+                                    dim3(kQuantWarps * 32), 0, s, 1, xb, T, I, valid_counts, qb,
+                                    scales, scale_ld));
       break;
     case BFQ_SCALE_F32_POW2:
-      silu_mul_quant_kernel<BFQ_SCALE_F32_POW2><<<grid, kQuantWarps * 32, 0, s>>>(
-          xb, T, I, valid_counts, qb, scales, scale_ld);
+      st = launch_status(launch_pdl(silu_mul_quant_kernel<BFQ_SCALE_F32_POW2>, grid,
+                                    dim3(kQuantWarps * 32), 0, s, 1, xb, T, I, valid_counts, qb,
+                                    scales, scale_ld));
       break;
     default:
-      silu_mul_quant_kernel<BFQ_SCALE_UE8M0_PACKED><<<grid, kQuantWarps * 32, 0, s>>>(
-          xb, T, I, valid_counts, qb, scales, scale_ld);
+      st = launch_status(launch_pdl(silu_mul_quant_kernel<BFQ_SCALE_UE8M0_PACKED>, grid,
+                                    dim3(kQuantWarps * 32), 0, s, 1, xb, T, I, valid_counts, qb,
+                                    scales, scale_ld));
       break;
   }
-  return launch_status(cudaGetLastError());
+  return st;
 }
 
 extern "C" bfq_status bfq_weight_block_quant(const void* w, int64_t batch, int64_t N,
@@ -343,11 +355,11 @@ extern "C" bfq_status bfq_weight_block_quant(const void* w, int64_t batch, int64
   if (st != BFQ_OK) return st;
   dim3 grid((unsigned)KB, (unsigned)NB, (unsigned)batch);
   cudaStream_t s = (cudaStream_t)stream;
+  const auto* wb = (const __nv_bfloat16*)w;
+  auto* wqb = (uint8_t*)wq;
   if (fmt == BFQ_SCALE_F32)
-    weight_quant_kernel<false><<<grid, 256, 0, s>>>((const __nv_bfloat16*)w, N, K,
-                                                    (uint8_t*)wq, sw);
-  else
-    weight_quant_kernel<true><<<grid, 256, 0, s>>>((const __nv_bfloat16*)w, N, K,
-                                                   (uint8_t*)wq, sw);
-  return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(weight_quant_kernel<false>, grid, dim3(256), 0, s, 1, wb, N,
+                                    K, wqb, sw));
+  return launch_status(launch_pdl(weight_quant_kernel<true>, grid, dim3(256), 0, s, 1, wb, N, K,
+                                  wqb, sw));
 }

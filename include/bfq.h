@@ -20,7 +20,12 @@
  *    library allocates nothing and frees nothing; it keeps no per-call state.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Work is enqueued asynchronously on it; the function returns as
- *    soon as the launch is enqueued.
+ *    soon as the launch is enqueued.  Kernels are launched with programmatic
+ *    stream serialization: a kernel may be scheduled while the previous one in
+ *    the stream is finishing, but it waits for that kernel's completion (and
+ *    memory visibility) before it reads or writes any global memory, so
+ *    stream order semantics are unchanged.  Launches can be captured in CUDA
+ *    graphs.
  *  - Arguments are validated on the host before anything is launched; an
  *    invalid call launches nothing and returns a non-zero bfq_status.  There
  *    is no CPU fallback and no alternative backend.
