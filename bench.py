@@ -68,6 +68,18 @@ def quant_alg_bytes(m, k):
     return 2 * m * k + m * k + (m + 3) // 4 * 4 * (k // 128) * 4
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The slowest rank's time (the job's time): all-reduce MAX over ranks.
+    Returns value unchanged when dist is None (one process)."""
+    if dist is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -517,11 +529,7 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    total_ms = start.elapsed_time(stop)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
 
     reps = max(3, min(args.steps, 20))
     qts, gts = timed_launches(bfq, torch, shapes, reps)
@@ -574,11 +582,7 @@ def run_gpu(args, rank, world, local_rank):
     pipe.join()
     e_stop.record()
     torch.cuda.synchronize()
-    e2e_ms = e_start.elapsed_time(e_stop)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_stop), dist, dev)
 
     if rank != 0:
         return 0

@@ -95,3 +95,49 @@ def test_masked_moe_config_sampled(cuda_lib, orc, N, K):
     experts = {nz[0], nz[len(nz) // 3], nz[2 * len(nz) // 3], nz[-1]}
     aq, sa, wq, sw, _ = _expert_problem(orc, E, T, N, K, cnt, 2, seed=N, experts=experts)
     _run_and_check(cuda_lib, orc, aq, sa, wq, sw, cnt, 2, experts=experts)
+
+
+def test_moe_expert_slice_chain(cuda_lib, orc):
+    """up GEMM -> silu-mul-quant -> down GEMM over masked experts, against the
+    oracle chain (the oracle's up result rounded to bf16, as the GPU stores
+    it).  Rows past each count stay untouched end to end."""
+    bfq = cuda_lib
+    E, T, H, I = 3, 136, 512, 256
+    cnt = np.array([70, 0, 136], np.int32)
+    x = synth.masked_activation(E, T, H, torch.from_numpy(cnt), seed=401, poison=False)
+    w_up = synth.expert_weights(E, 2 * I, H, seed=402)
+    w_dn = synth.expert_weights(E, H, I, seed=403)
+    d_cnt = torch.from_numpy(cnt).cuda()
+    # GPU chain
+    a_up = torch.zeros((E, T, H), dtype=torch.float8_e4m3fn, device="cuda")
+    sa_up = torch.zeros((E, bfq.scale_cols(H, 2), T), dtype=torch.int32, device="cuda")
+    for e in range(E):
+        if cnt[e]:
+            bfq.bfq_quant(x[e, :cnt[e]].cuda(), a_up[e, :cnt[e]], sa_up[e], 2, T)
+    wq_up, sw_up = bfq.weight_block_quant(w_up.cuda(), 1)
+    wq_dn, sw_dn = bfq.weight_block_quant(w_dn.cuda(), 1)
+    h = torch.full((E, T, 2 * I), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bfq.gemm_masked(a_up, sa_up, 2, wq_up, sw_up, d_cnt, out=h)
+    a_dn, sa_dn = bfq.silu_mul_quant(h, d_cnt, 2)
+    out = torch.full((E, T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bfq.gemm_masked(a_dn, sa_dn, 2, wq_dn, sw_dn, d_cnt, out=out)
+    torch.cuda.synchronize()
+    oh = out.float().cpu().numpy()
+    # oracle chain
+    for e in range(E):
+        c = int(cnt[e])
+        assert np.isnan(oh[e, c:]).all()
+        if c == 0:
+            continue
+        oq, osa = orc.quant(bits(x[e, :c]), 2, scale_ld=T)
+        owq, osw = orc.weight_block_quant(bits(w_up[e]), True)
+        up = orc.gemm(oq, osa, 2, owq, osw)                       # fp64 [c, 2I]
+        h_bits = bits(torch.from_numpy(up).to(torch.bfloat16))     # bf16 RNE, as stored
+        hq, hs = orc.silu_mul_quant(h_bits.reshape(1, c, 2 * I), np.array([c], np.int32), 2,
+                                    scale_ld=T)
+        dq, dsw = orc.weight_block_quant(bits(w_dn[e]), True)
+        ref = orc.gemm(hq[0], hs[0], 2, dq, dsw)
+        an = np.linalg.norm(orc.dequant_rows(hq[0], hs[0], 2), axis=1)
+        wn = np.linalg.norm(orc.dequant_weight(dq, dsw), axis=1)
+        err = np.abs(oh[e, :c] - ref) / (an[:, None] * wn[None, :])
+        assert np.isfinite(oh[e, :c]).all() and err.max() <= 2e-3, (e, float(err.max()))
