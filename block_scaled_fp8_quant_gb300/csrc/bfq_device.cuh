@@ -451,6 +451,65 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
   return f;
 }
 
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// Packed f32x2 arithmetic: each lane of the pair is rounded exactly as the
+// scalar fp32 operation (round to nearest even, subnormals kept).
+__device__ __forceinline__ uint64_t fma2_rn(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2_rn(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2_rn(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// bfq_silu on two values at once: the same fp32 operations as bfq_expf and
+// bfq_silu in the same order (so bit-identical results), with the
+// multiplies and FMAs of the range reduction, the polynomial and the
+// scaling issued as f32x2 pairs, and the range cases of bfq_expf applied by
+// selection afterwards.
+__device__ __forceinline__ float exp_range_fix(float x, float v) {
+  return isnan(x) ? x : (x < -88.0f ? 0.0f : (x > 89.0f ? __int_as_float(0x7F800000) : v));
+}
+
+__device__ __forceinline__ float2 bfq_silu2(float g0, float g1) {
+  const float x0 = -g0, x1 = -g1;
+  const uint64_t x = pack2(x0, x1);
+  const float2 t = unpack2(mul2_rn(x, splat2(0x1.715476p+0f)));
+  const float n0 = rintf(t.x), n1 = rintf(t.y);
+  const uint64_t n = pack2(n0, n1);
+  // fma(-n, c, x) == fma(n, -c, x) exactly
+  uint64_t r = fma2_rn(n, splat2(-0x1.62e4p-1f), x);
+  r = fma2_rn(n, splat2(-0x1.7f7d1cp-20f), r);
+  uint64_t p = splat2(0x1.a01a02p-13f);
+  p = fma2_rn(p, r, splat2(0x1.6c16c2p-10f));
+  p = fma2_rn(p, r, splat2(0x1.111112p-7f));
+  p = fma2_rn(p, r, splat2(0x1.555556p-5f));
+  p = fma2_rn(p, r, splat2(0x1.555556p-3f));
+  p = fma2_rn(p, r, splat2(0.5f));
+  p = fma2_rn(p, r, splat2(1.0f));
+  p = fma2_rn(p, r, splat2(1.0f));
+  const int k0 = (int)n0, k1 = (int)n1;
+  const int h0 = k0 / 2, h1 = k1 / 2;
+  const float2 e = unpack2(mul2_rn(mul2_rn(p, pack2(pow2_int(h0), pow2_int(h1))),
+                                   pack2(pow2_int(k0 - h0), pow2_int(k1 - h1))));
+  const float2 d =
+      unpack2(add2_rn(pack2(exp_range_fix(x0, e.x), exp_range_fix(x1, e.y)), splat2(1.0f)));
+  return make_float2(__fdiv_rn(g0, d.x), __fdiv_rn(g1, d.y));
+}
+
 // 4-byte asynchronous global -> shared copy (no register round trip).
 __device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src)

@@ -479,10 +479,12 @@ size_t split_ws_bytes(int64_t M, int64_t N, int splits) {
 template <int BN>
 int max_active_clusters(const DeviceInfo& dev, int cluster);
 
-Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, size_t ws_avail,
-                bool limit_by_ws) {
+// Plan for one tile width: K is split over a cluster of CTAs when there are
+// fewer tiles than SMs.
+Plan plan_for_width(const DeviceInfo& dev, int bn, int64_t M, int64_t N, int64_t K,
+                    size_t ws_avail, bool limit_by_ws) {
   Plan pl;
-  pl.bn = N > 128 ? 256 : 128;
+  pl.bn = bn;
   pl.m_tiles = (int)cdiv(M, kBM);
   pl.n_tiles = (int)cdiv(N, pl.bn);
   const int tiles = pl.m_tiles * pl.n_tiles;
@@ -500,6 +502,24 @@ Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, size_t w
     while (splits > 1 && split_ws_bytes(M, N, splits) > ws_avail) --splits;
   pl.splits = splits;
   pl.ws_bytes = split_ws_bytes(M, N, splits);
+  return pl;
+}
+
+// 256-wide tiles, except where 128-wide tiles need no K split at all and
+// keep at least as many CTAs busy: that drops the fp32 partial sums a split
+// tile writes and its cluster reads back (splits x M x N x 4 bytes each way)
+// and lets the tile leave through the TMA-store epilogue.  This pays once the
+// tile holds more than 32 rows; with fewer rows the partials are small and
+// the 256-wide tile's larger weight stages (more bytes in flight per SM) win.
+Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, size_t ws_avail,
+                bool limit_by_ws) {
+  Plan pl = plan_for_width(dev, N > 128 ? 256 : 128, M, N, K, ws_avail, limit_by_ws);
+  if (pl.bn == 256 && pl.splits > 1 && M > 32) {
+    const Plan alt = plan_for_width(dev, 128, M, N, K, ws_avail, limit_by_ws);
+    if (alt.splits == 1 &&
+        alt.m_tiles * alt.n_tiles >= pl.m_tiles * pl.n_tiles * pl.splits)
+      pl = alt;
+  }
   return pl;
 }
 

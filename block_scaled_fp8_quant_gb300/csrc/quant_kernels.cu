@@ -135,7 +135,11 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 // ---------------------------------------------------------------------------
 // fused silu-and-mul + quant over a masked per-expert batch
 // ---------------------------------------------------------------------------
-constexpr int kSiluRowsPerBlock = 8;
+// Two rows per block and one unit in flight per warp: the kernel is bound by
+// the exp and division of silu, and small blocks keep more warps resident
+// (fewer registers each) and spread the valid rows evenly over the SMs.
+constexpr int kSiluRowsPerBlock = 2;
+constexpr int kSiluUnroll = 1;
 
 template <int FMT>
 __global__ void __launch_bounds__(kQuantWarps * 32)
@@ -161,11 +165,11 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
                    ? (void*)((uint32_t*)scales + (int64_t)e * cols * scale_ld)
                    : (void*)((float*)scales + (int64_t)e * cols * scale_ld);
 
-  for (int u0 = warp * kUnroll; u0 < units; u0 += kQuantWarps * kUnroll) {
-    uint4 raw[kUnroll][4];
-    bool act[kUnroll];
+  for (int u0 = warp * kSiluUnroll; u0 < units; u0 += kQuantWarps * kSiluUnroll) {
+    uint4 raw[kSiluUnroll][4];
+    bool act[kSiluUnroll];
 #pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
+    for (int j = 0; j < kSiluUnroll; ++j) {
       const int u = u0 + j;
       const int r = r0 + u / chunks, c = u % chunks;
       act[j] = (u < units) && (c * 4 + gl < G);
@@ -181,7 +185,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       }
     }
 #pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
+    for (int j = 0; j < kSiluUnroll; ++j) {
       const int u = u0 + j;
       if (u >= units) break;
       const int r = r0 + u / chunks, c = u % chunks;
@@ -189,7 +193,12 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       unpack16(raw[j][0], raw[j][1], g);
       unpack16(raw[j][2], raw[j][3], up);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(bfq_silu(g[i]), up[i]);
+      for (int i = 0; i < 16; i += 2) {
+        const float2 sg = bfq_silu2(g[i], g[i + 1]);
+        const float2 yy = unpack2(mul2_rn(pack2(sg.x, sg.y), pack2(up[i], up[i + 1])));
+        y[i] = yy.x;
+        y[i + 1] = yy.y;
+      }
       uint4 codes;
       const float s = quant16<FMT>(y, codes);
       if (act[j]) st_v4(q + ((int64_t)e * T + r) * I + c * 512 + lane * 16, codes);

@@ -141,3 +141,22 @@ def test_gemm_parity_unsplit_many_tiles(cuda_lib, orc, fmt, M, N, K):
     ref = orc.gemm(aq, sa, fmt, wq, sw)
     an, wn = _norms(orc, aq, sa, wq, sw, fmt)
     assert_gemm_close(out.float().cpu().numpy(), ref, an, wn, f"unsplit {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fmt", [0, 2])
+@pytest.mark.parametrize("M,N,K", [(40, 13056, 256), (100, 16384, 256)])
+def test_gemm_parity_narrow_unsplit_plan(cuda_lib, orc, fmt, M, N, K):
+    """One row tile of more than 32 rows whose 256-wide plan would split K
+    two ways: the plan takes 128-wide tiles with no split instead (no
+    workspace on a 152-SM GB300)."""
+    bfq = cuda_lib
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert bfq.bfq_gemm_workspace_bytes(M, N, K) == 0
+    aq, sa, wq, sw = _oracle_problem(orc, M, N, K, fmt, seed=M + N + K + fmt)
+    d = _to_dev(aq, sa, wq, sw, fmt)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bfq.gemm(d[0], d[1], fmt, d[2], d[3], out=out)
+    torch.cuda.synchronize()
+    ref = orc.gemm(aq, sa, fmt, wq, sw)
+    an, wn = _norms(orc, aq, sa, wq, sw, fmt)
+    assert_gemm_close(out.float().cpu().numpy(), ref, an, wn, f"narrow {M}x{N}x{K}")
