@@ -235,6 +235,17 @@ __device__ __forceinline__ void bulk_commit_and_wait_all() {
   asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Close the current bulk async-group (TMA stores issued so far).
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until every committed bulk store has finished reading its shared
+// memory source (the global writes may still be in flight).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA) before a barrier.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -531,6 +542,19 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 template <int N>
 __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32), id 1..15, that
+// returns in every participating thread whether any of them passed true.
+__device__ __forceinline__ bool named_barrier_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // Named barrier over `count` threads (a multiple of 32), id 1..15.

@@ -42,18 +42,27 @@ constexpr int kMaxSplits = 8;  // K splits of a tile form one (portable-size) cl
 // the allocation the kernel is launched with (checked on the host).
 // Warp 2 streams the scales into shared memory.  BN = 128: seven warps, two
 // per sub-partition at most, no reconfiguration.
-template <int BN>
+// BN = 128 with MINB = 2 ("paired"): two CTAs share an SM so that one CTA's
+// set-up, pipeline fill and epilogue overlap the other's main loop.  Each
+// holds half the SM's registers, TMEM and shared memory: two warpgroups
+// (warpgroup 0 at 24 registers, the four epilogue warps at 232:
+// 128*24 + 128*232 = 32768 = 256 threads * 128), a 3-stage ring (~102 KB)
+// and 256 TMEM columns; the epilogue reads TMEM 32 columns at a time.
+template <int BN, int MINB = 1>
 struct GemmCfg {
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr bool kPaired = (MINB == 2);
+  static_assert(MINB == 1 || (MINB == 2 && BN == 128), "two CTAs per SM only with BN = 128");
+  static constexpr int kStages = (BN == 256) ? 4 : (kPaired ? 3 : 6);
   static constexpr int kEpiWarps = BN / 32;  // 128 columns per warp
-  static constexpr int kEpiWarp0 = (BN == 256) ? 4 : 3;
+  static constexpr int kEpiWarp0 = (BN == 256 || kPaired) ? 4 : 3;
   static constexpr int kScaleWarp = 2;       // streams the scales into smem
   static constexpr int kScaleSlots = 8;      // K blocks of scales in flight
   static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
-  static constexpr bool kRegSplit = (BN == 256);
-  static constexpr int kLaunchRegs = 168;
+  static constexpr bool kRegSplit = (BN == 256) || kPaired;
+  static constexpr int kLaunchRegs = kPaired ? 128 : 168;
   static constexpr int kProducerRegs = 24;
-  static constexpr int kEpilogueRegs = 240;
+  static constexpr int kEpilogueRegs = kPaired ? 232 : 240;
+  static constexpr int kLdCols = kPaired ? 32 : 64;  // TMEM columns per tcgen05.ld
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -80,6 +89,7 @@ struct GemmParams {
   int N, K;
   int m_tiles, n_tiles, splits;
   int a_fmt;
+  int E;                   // masked: experts
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -87,12 +97,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int BN, bool MASKED>
-__global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
+template <int BN, bool MASKED, int MINB = 1>
+__global__ void __launch_bounds__(GemmCfg<BN, MINB>::kThreads, MINB)
     gemm_block_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmW,
                           const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, MINB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
@@ -163,7 +173,8 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
   // touch global memory before that kernel has finished.
   if (!MASKED) griddep_wait();
   griddep_launch_dependents();
-  static_assert(!C::kRegSplit || 128 * C::kProducerRegs + 256 * C::kEpilogueRegs <=
+  static_assert(!C::kRegSplit || 128 * C::kProducerRegs +
+                                         (C::kThreads - 128) * C::kEpilogueRegs <=
                                      C::kThreads * C::kLaunchRegs,
                 "register split exceeds the launch allocation");
 
@@ -296,12 +307,22 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
       if (warp_active) {
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                (uint32_t)(buf * BN + half * 128);
+        if constexpr (C::kLdCols == 64) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint64_t v[32];
-          tmem_ld64_pairs_wait(taddr + (uint32_t)(h * 64), v);
+          for (int h = 0; h < 2; ++h) {
+            uint64_t v[32];
+            tmem_ld64_pairs_wait(taddr + (uint32_t)(h * 64), v);
 #pragma unroll
-          for (int t = 0; t < 32; ++t) ffma2(acc[h * 32 + t], v[t], s2);
+            for (int t = 0; t < 32; ++t) ffma2(acc[h * 32 + t], v[t], s2);
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            uint64_t v[16];
+            tmem_ld32_pairs_wait(taddr + (uint32_t)(h * 32), v);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) ffma2(acc[h * 16 + t], v[t], s2);
+          }
         }
       }
       tc_fence_before_sync();
@@ -408,6 +429,391 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
   }
 }
 
+
+// ----------------------------------------------------------------------------
+// Persistent form (BN = 256, no K split): one CTA per SM walks its share of
+// the tiles, tile t going to CTA t mod gridDim.x.  The TMA producer, the MMA
+// issuer and the scale loader run ahead across tile boundaries, so a tile's
+// promotion drain and store overlap the next tile's loads and first MMAs, and
+// barrier and TMEM set-up are paid once per SM rather than once per tile.
+// Dense tiles leave through a dedicated 16 KB staging buffer, one 128 x 64
+// TMA-store box at a time (the stage ring stays busy with the next tile).
+// Masked: the tile list holds only row tiles that start below their expert's
+// count — per-expert tile counts are prefix-summed in shared memory at start
+// — so padding costs no CTA time and the valid tiles spread evenly over the
+// SMs; rows past the count are never written.
+// ----------------------------------------------------------------------------
+constexpr int kPersistMaxExperts = 1024;
+
+struct PersistCfg {
+  using C = GemmCfg<256>;
+  static constexpr int kStagingBytes = kBM * 64 * 2;  // one 128-row x 64-column bf16 box
+  static constexpr int kPrefixBytes = (2 * kPersistMaxExperts + 2) * 4;
+  static constexpr size_t kSmemBytes = (size_t)C::kStages * C::kStageBytes + kStagingBytes +
+                                       C::kScaleBytes + kPrefixBytes + C::kBarrierBytes + 1024;
+  // Register split of the 384-thread launch (168 each): warpgroup 0 keeps 40
+  // (its tile walk spills at 24, which slowed every K block by ~30 %), the
+  // epilogue 232 (no spills).
+  static constexpr int kWg0Regs = 40;
+  static constexpr int kEpiRegs = 232;
+  static_assert(128 * kWg0Regs + 256 * kEpiRegs <= 384 * 168, "register split");
+};
+
+// Tile t of the persistent schedule -> (expert, first row, first column,
+// valid rows of the expert).  Masked: tpre[e] = tiles of experts < e,
+// cnt[e] = clamped valid rows of expert e.
+template <bool MASKED>
+__device__ __forceinline__ void persist_tile(int t, const GemmParams& p, const int* tpre,
+                                             const int* cnt, int& e, int& m0, int& n0,
+                                             int& m_limit) {
+  if (MASKED) {
+    int lo = 0, hi = p.E;  // tpre[lo] <= t < tpre[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tpre[mid] <= t) lo = mid;
+      else hi = mid;
+    }
+    e = lo;
+    m_limit = cnt[e];
+    const int a = (m_limit + kBM - 1) / kBM;  // active row tiles of expert e
+    const int r = t - tpre[e];
+    const int nt = r / a;
+    m0 = (r - nt * a) * kBM;
+    n0 = nt * 256;
+  } else {
+    e = 0;
+    m_limit = p.M;
+    const int nt = t / p.m_tiles;
+    m0 = (t - nt * p.m_tiles) * kBM;
+    n0 = nt * 256;
+  }
+}
+
+template <bool MASKED>
+__global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
+    gemm_block_fp8_persistent(const __grid_constant__ CUtensorMap tmA,
+                              const __grid_constant__ CUtensorMap tmW,
+                              const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
+  constexpr int BN = 256;
+  using C = GemmCfg<BN>;
+  using PC = PersistCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::kStages * C::kABytes;
+  uint8_t* stg = smem + (size_t)C::kStages * C::kStageBytes;  // 1024-byte aligned
+  uint32_t* sc_a = (uint32_t*)(stg + PC::kStagingBytes);       // [slot][128]
+  uint32_t* sc_w = sc_a + C::kScaleSlots * kBM;                // [slot][2]
+  int* tpre = (int*)(sc_w + 2 * C::kScaleSlots);               // [E + 1]
+  int* cnt = tpre + kPersistMaxExperts + 1;                    // [E]
+  uint64_t* full = (uint64_t*)(cnt + kPersistMaxExperts + 1);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* sfull = tempty + 2;
+  uint64_t* sempty = sfull + C::kScaleSlots;
+  uint64_t* drain = sempty + C::kScaleSlots;
+  uint32_t* tmem_slot = (uint32_t*)(drain + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KB = p.K / kBK;
+
+  if (MASKED) {
+    // per-expert tile counts, then an exclusive prefix sum by warp 0
+    griddep_wait();  // the counts may come from the previous kernel
+    for (int x = threadIdx.x; x < p.E; x += blockDim.x) {
+      int c = __ldg(p.counts + x);
+      c = c < 0 ? 0 : (c > p.M ? p.M : c);
+      cnt[x] = c;
+      tpre[x + 1] = (c + kBM - 1) / kBM * p.n_tiles;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int per = (p.E + 31) / 32;
+      const int b = lane * per;
+      const int b_end = min(p.E, b + per);
+      int sum = 0;
+      for (int x = b; x < b_end; ++x) sum += tpre[x + 1];
+      int inc = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      int run = inc - sum;
+      for (int x = b; x < b_end; ++x) {
+        run += tpre[x + 1];
+        tpre[x + 1] = run;
+      }
+      if (lane == 0) tpre[0] = 0;
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], C::kEpiWarps);
+    }
+    for (int b = 0; b < C::kScaleSlots; ++b) {
+      mbar_init(&sfull[b], 32);
+      mbar_init(&sempty[b], C::kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmW);
+    if (!MASKED) prefetch_tensormap(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  if (!MASKED) griddep_wait();
+  griddep_launch_dependents();
+  const int total = MASKED ? tpre[p.E] : p.m_tiles * p.n_tiles;
+
+  // Tiles of this CTA and the K blocks they stream, as one flat sequence
+  // g = 0 .. steps-1 (tile g / KB, K block g mod KB): the warps that run at
+  // 24 registers keep only a counter and the current tile's coordinates.
+  const int my_tiles = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int steps = my_tiles * KB;
+  static_assert((C::kStages & (C::kStages - 1)) == 0 && C::kStages == 4, "ring of 4 stages");
+  static_assert(C::kScaleSlots == 8, "scale ring of 8 slots");
+
+  if (warp < C::kEpiWarp0) {
+    setmaxnreg_dec<PC::kWg0Regs>();
+    if (warp == 0) {
+      // ------------------------------ TMA producer ------------------------------
+      if (lane == 0) {
+        int g = 0, i = 0, t = blockIdx.x, a_row = 0, w_row = 0;
+        for (; g < steps; ++g) {
+          if (i == 0) {
+            int e, m0, n0, ml;
+            persist_tile<MASKED>(t, p, tpre, cnt, e, m0, n0, ml);
+            a_row = (MASKED ? e * p.M : 0) + m0;
+            w_row = (MASKED ? e * p.N : 0) + n0;
+          }
+          const int s = g & 3;
+          const uint32_t ph = (uint32_t)(g >> 2) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)C::kStageBytes);
+          tma_load_2d_nohint(sA + (size_t)s * C::kABytes, &tmA, &full[s], i * kBK, a_row);
+          tma_load_2d_nohint(sB + (size_t)s * C::kBBytes, &tmW, &full[s], i * kBK, w_row);
+          if (++i == KB) {
+            i = 0;
+            t += gridDim.x;
+          }
+        }
+        if (*abort_flag) {
+          // let the copies already issued land before the CTA can exit
+          for (int j = g - C::kStages < 0 ? 0 : g - C::kStages; j < g; ++j) {
+            volatile int no_abort = 0;
+            (void)mbar_wait(&full[j & 3], (uint32_t)(j >> 2) & 1u, &no_abort, p.status,
+                            kWaitTimeoutNs / 8);
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------- MMA issuer -------------------------------
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+        int g = 0;
+        for (; g < steps; ++g) {
+          const int s = g & 3;
+          const int buf = g & 1;
+          if (!mbar_wait(&tempty[buf], ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag, p.status,
+                         kWaitTimeoutNs))
+            break;
+          tc_fence_after_sync();
+          if (!mbar_wait(&full[s], (uint32_t)(g >> 2) & 1u, abort_flag, p.status, kWaitTimeoutNs))
+            break;
+          tc_fence_after_sync();
+          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + (size_t)s * C::kABytes));
+          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + (size_t)s * C::kBBytes));
+          const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            umma_e4m3(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                      kk > 0 ? 1u : 0u);
+          umma_commit(&empty[s]);
+          umma_commit(&tfull[buf]);
+        }
+        if (*abort_flag && g > 0) {
+          // wait for the MMAs already issued before TMEM is released
+          umma_commit(drain);
+          volatile int no_abort = 0;
+          (void)mbar_wait(drain, 0, &no_abort, p.status, kWaitTimeoutNs / 8);
+        }
+      }
+    } else if (warp == C::kScaleWarp) {
+      // ------------------------------ scale loader ------------------------------
+      const int nblks = (int)((p.N + 127) / 128);
+      const bool packed = p.a_fmt == BFQ_SCALE_UE8M0_PACKED;
+      const uint32_t* sa = (const uint32_t*)p.sa;
+      const float* sw = p.sw;
+      int i = 0, t = blockIdx.x, m0 = 0, ml = 0, nb0 = 0;
+      for (int g = 0; g < steps; ++g) {
+        if (i == 0) {
+          int e, n0;
+          persist_tile<MASKED>(t, p, tpre, cnt, e, m0, n0, ml);
+          sa = (const uint32_t*)p.sa + (MASKED ? (int64_t)e * p.sa_estride : 0);
+          sw = p.sw + (MASKED ? (int64_t)e * p.sw_estride : 0);
+          nb0 = n0 / 128;
+        }
+        const int slot = g & 7;
+        if (!mbar_wait(&sempty[slot], ((uint32_t)(g >> 3) & 1u) ^ 1u, abort_flag, p.status,
+                       kWaitTimeoutNs))
+          break;
+        const uint32_t* col = sa + (int64_t)(packed ? (i >> 2) : i) * p.sa_ld;
+#pragma unroll
+        for (int r = lane; r < kBM; r += 32)
+          if (m0 + r < ml) cp_async_4(&sc_a[slot * kBM + r], col + m0 + r);
+        if (lane < 2 && nb0 + lane < nblks)
+          cp_async_4(&sc_w[slot * 2 + lane], sw + (int64_t)(nb0 + lane) * KB + i);
+        cp_async_arrive_noinc(&sfull[slot]);
+        if (++i == KB) {
+          i = 0;
+          t += gridDim.x;
+        }
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+    __syncwarp();
+  } else {
+    setmaxnreg_inc<PC::kEpiRegs>();
+    // ------------------------- epilogue / promotion ---------------------------
+    const int ew = warp - C::kEpiWarp0;
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int half = ew >> 2;
+    const int row_local = quarter * 32 + lane;
+    const bool store_thread = threadIdx.x == C::kEpiWarp0 * 32;
+    int g = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int e, m0, n0, m_limit;
+      persist_tile<MASKED>(t, p, tpre, cnt, e, m0, n0, m_limit);
+      const int m = m0 + row_local;
+      const bool row_ok = m < m_limit;
+      const int col0 = n0 + half * 128;
+      const bool warp_active = (m0 + quarter * 32 < m_limit) && (col0 < p.N);
+      const int ncols = min(128, p.N - col0);
+
+      uint64_t acc[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[j] = 0ull;
+      bool stop = false;
+      for (int i = 0; i < KB; ++i, ++g) {
+        const int buf = g & 1;
+        const uint32_t tph = (uint32_t)(g >> 1) & 1u;
+        const int slot = g & 7;
+        const uint32_t sph = (uint32_t)(g >> 3) & 1u;
+        if (!mbar_wait(&sfull[slot], sph, abort_flag, p.status, kWaitTimeoutNs)) {
+          stop = true;
+          break;
+        }
+        const uint32_t a_bits = sc_a[slot * kBM + row_local];
+        const float w_s = __uint_as_float(sc_w[slot * 2 + half]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sempty[slot]);
+        float sa_v;
+        if (p.a_fmt == BFQ_SCALE_UE8M0_PACKED) {
+          const uint32_t b = (a_bits >> (8 * (i & 3))) & 0xFFu;
+          sa_v = b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);  // 2^(b-127)
+        } else {
+          sa_v = __uint_as_float(a_bits);
+        }
+        const uint64_t s2 = splat2(__fmul_rn(row_ok ? sa_v : 0.0f, w_s));
+        if (!mbar_wait(&tfull[buf], tph, abort_flag, p.status, kWaitTimeoutNs)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after_sync();
+        if (warp_active) {
+          const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                 (uint32_t)(buf * BN + half * 128);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint64_t v[32];
+            tmem_ld64_pairs_wait(taddr + (uint32_t)(h * 64), v);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) ffma2(acc[h * 32 + q], v[q], s2);
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+      }
+      // Every epilogue warp takes the same decision (the dense store below
+      // synchronises them on named barriers).
+      if (MASKED) {
+        if (stop || *abort_flag) break;
+      } else if (named_barrier_or(2, C::kEpiWarps * 32, stop || *abort_flag)) {
+        break;
+      }
+
+      if (MASKED) {
+        if (warp_active && row_ok) {
+          __nv_bfloat16* dst = p.out + (int64_t)e * p.out_estride + (int64_t)m * p.N + col0;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            if (c * 8 < ncols) {
+              const float2 f0 = unpack2(acc[c * 4 + 0]), f1 = unpack2(acc[c * 4 + 1]);
+              const float2 f2 = unpack2(acc[c * 4 + 2]), f3 = unpack2(acc[c * 4 + 3]);
+              st_v4(dst + c * 8, make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
+                                            pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
+            }
+          }
+        }
+      } else {
+        // Four 128 x 64 boxes through the staging buffer (128-byte swizzle,
+        // 16-byte chunk c of row r at chunk c ^ (r mod 8)); rows >= M are
+        // clipped by the tensor map.
+#pragma unroll
+        for (int blk = 0; blk < BN / 64; ++blk) {
+          if (store_thread) bulk_wait_read_all();  // previous box has left the buffer
+          named_barrier(1, C::kEpiWarps * 32);
+          if (half == (blk >> 1) && warp_active) {
+            const uint32_t row_addr = smem_u32(stg) + (uint32_t)(row_local * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int a = (blk & 1) * 32 + c * 4;  // pair index of column (blk&1)*64 + c*8
+              const float2 f0 = unpack2(acc[a + 0]), f1 = unpack2(acc[a + 1]);
+              const float2 f2 = unpack2(acc[a + 2]), f3 = unpack2(acc[a + 3]);
+              st_shared_v4(row_addr + (uint32_t)((c ^ (row_local & 7)) << 4),
+                           make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
+                                      pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
+            }
+          }
+          fence_proxy_async_smem();
+          named_barrier(1, C::kEpiWarps * 32);
+          if (store_thread && n0 + blk * 64 < p.N) {
+            tma_store_2d(&tmO, stg, n0 + blk * 64, m0);
+            bulk_commit();
+          }
+        }
+      }
+    }
+    if (!MASKED && store_thread) bulk_wait_read_all();
+  }
+
+  // ---- teardown: everyone is done with TMEM before it is released ----
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
 // ----------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------
@@ -464,6 +870,8 @@ bool make_out_map(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows) {
 
 struct Plan {
   int bn = 256;
+  int minb = 1;          // CTAs per SM (2: the paired 128-wide configuration)
+  bool persist = false;  // persistent 256-wide kernel (no K split)
   int m_tiles = 0, n_tiles = 0, splits = 1;
   size_t ws_bytes = 0;  // bytes needed by this plan
 };
@@ -520,12 +928,16 @@ Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, size_t w
         alt.m_tiles * alt.n_tiles >= pl.m_tiles * pl.n_tiles * pl.splits)
       pl = alt;
   }
+  // More 256-wide tiles than SMs: one persistent CTA per SM walks them.
+  if (pl.bn == 256 && pl.splits == 1 && pl.m_tiles * pl.n_tiles > dev.sm_count &&
+      dev.smem_optin >= PersistCfg::kSmemBytes)
+    pl.persist = true;
   return pl;
 }
 
-template <int BN, bool MASKED>
+template <int BN, bool MASKED, int MINB = 1>
 bfq_status configure(const DeviceInfo& dev) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, MINB>;
   static bool configured[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
@@ -534,15 +946,21 @@ bfq_status configure(const DeviceInfo& dev) {
     // setmaxnreg.inc only completes if the launch allocation covers the
     // split; refuse to launch a build whose register count differs.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, gemm_block_fp8_kernel<BN, MASKED>) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, gemm_block_fp8_kernel<BN, MASKED, MINB>) != cudaSuccess) {
       cudaGetLastError();
       return BFQ_ERR_CUDA;
     }
     if (fa.numRegs != C::kLaunchRegs) return BFQ_ERR_DEVICE;
   }
-  if (cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED>,
+  if (cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED, MINB>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)C::kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return BFQ_ERR_CUDA;
+  }
+  if (C::kPaired && cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED, MINB>,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
     cudaGetLastError();
     return BFQ_ERR_CUDA;
   }
@@ -585,15 +1003,60 @@ int max_active_clusters(const DeviceInfo& dev, int cluster) {
   return n;
 }
 
-template <int BN, bool MASKED>
+template <int BN, bool MASKED, int MINB = 1>
 bfq_status launch(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
                   const CUtensorMap& mo, const GemmParams& p, unsigned grid, cudaStream_t s) {
-  using C = GemmCfg<BN>;
-  bfq_status st = configure<BN, MASKED>(dev);
+  using C = GemmCfg<BN, MINB>;
+  bfq_status st = configure<BN, MASKED, MINB>(dev);
   if (st != BFQ_OK) return st;
-  return launch_status(launch_pdl(gemm_block_fp8_kernel<BN, MASKED>, dim3(grid),
+  return launch_status(launch_pdl(gemm_block_fp8_kernel<BN, MASKED, MINB>, dim3(grid),
                                   dim3(C::kThreads), C::kSmemBytes, s,
                                   p.splits > 1 ? (unsigned)p.splits : 1u, ma, mw, mo, p));
+}
+
+// Tile configuration of the masked grouped GEMM (no K split).
+Plan masked_plan(const DeviceInfo& dev, int64_t E, int64_t T, int64_t N, int64_t K) {
+  (void)T;
+  (void)K;
+  Plan pl;
+  pl.bn = N > 128 ? 256 : 128;
+  pl.persist = pl.bn == 256 && E <= kPersistMaxExperts &&
+               dev.smem_optin >= PersistCfg::kSmemBytes;
+  return pl;
+}
+
+template <bool MASKED>
+bfq_status configure_persistent(const DeviceInfo& dev) {
+  static bool configured[64] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (configured[dev.ordinal]) return BFQ_OK;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, gemm_block_fp8_persistent<MASKED>) != cudaSuccess) {
+    cudaGetLastError();
+    return BFQ_ERR_CUDA;
+  }
+  // setmaxnreg.inc only completes if the launch allocation covers the split
+  if (fa.numRegs != GemmCfg<256>::kLaunchRegs) return BFQ_ERR_DEVICE;
+  if (cudaFuncSetAttribute(gemm_block_fp8_persistent<MASKED>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)PersistCfg::kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return BFQ_ERR_CUDA;
+  }
+  configured[dev.ordinal] = true;
+  return BFQ_OK;
+}
+
+template <bool MASKED>
+bfq_status launch_persistent(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
+                             const CUtensorMap& mo, const GemmParams& p, unsigned grid,
+                             cudaStream_t s) {
+  bfq_status st = configure_persistent<MASKED>(dev);
+  if (st != BFQ_OK) return st;
+  return launch_status(launch_pdl(gemm_block_fp8_persistent<MASKED>, dim3(grid),
+                                  dim3(GemmCfg<256>::kThreads), PersistCfg::kSmemBytes, s, 1u, ma,
+                                  mw, mo, p));
 }
 
 bfq_status check_device(DeviceInfo* dev) {
@@ -658,7 +1121,11 @@ extern "C" bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, 
   if (pl.splits > 1) p.ws = (float*)workspace;
   const unsigned grid = (unsigned)(pl.m_tiles * pl.n_tiles * pl.splits);
   cudaStream_t s = (cudaStream_t)stream;
-  return pl.bn == 256 ? launch<256, false>(dev, ma, mw, mo, p, grid, s)
+  if (pl.persist)
+    return launch_persistent<false>(dev, ma, mw, mo, p, grid < (unsigned)dev.sm_count
+                                                           ? grid : (unsigned)dev.sm_count, s);
+  if (pl.bn == 256) return launch<256, false>(dev, ma, mw, mo, p, grid, s);
+  return pl.minb == 2 ? launch<128, false, 2>(dev, ma, mw, mo, p, grid, s)
                       : launch<128, false>(dev, ma, mw, mo, p, grid, s);
 }
 
@@ -684,7 +1151,8 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked(
   DeviceInfo dev;
   bfq_status st = check_device(&dev);
   if (st != BFQ_OK) return st;
-  const int bn = N > 128 ? 256 : 128;
+  const Plan mp = masked_plan(dev, E, T, N, K);
+  const int bn = mp.bn;
   CUtensorMap ma, mw;
   if (!make_map(&ma, a_q, (uint64_t)K, (uint64_t)E * T, kBM) ||
       !make_map(&mw, w_q, (uint64_t)K, (uint64_t)E * N, (uint32_t)bn))
@@ -707,11 +1175,16 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked(
   p.n_tiles = (int)cdiv(N, bn);
   p.splits = 1;
   p.a_fmt = a_fmt;
+  p.E = E;
   const int64_t grid = (int64_t)p.m_tiles * p.n_tiles * E;
   if (grid > 0x7FFFFFFF) return BFQ_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;
-  return bn == 256 ? launch<256, true>(dev, ma, mw, mw, p, (unsigned)grid, s)
-                   : launch<128, true>(dev, ma, mw, mw, p, (unsigned)grid, s);
+  if (mp.persist)
+    return launch_persistent<true>(dev, ma, mw, mw, p,
+                                   (unsigned)(grid < dev.sm_count ? grid : dev.sm_count), s);
+  if (bn == 256) return launch<256, true>(dev, ma, mw, mw, p, (unsigned)grid, s);
+  return mp.minb == 2 ? launch<128, true, 2>(dev, ma, mw, mw, p, (unsigned)grid, s)
+                      : launch<128, true>(dev, ma, mw, mw, p, (unsigned)grid, s);
 }
 
 // ----------------------------------------------------------------------------

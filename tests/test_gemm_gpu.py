@@ -160,3 +160,27 @@ def test_gemm_parity_narrow_unsplit_plan(cuda_lib, orc, fmt, M, N, K):
     ref = orc.gemm(aq, sa, fmt, wq, sw)
     an, wn = _norms(orc, aq, sa, wq, sw, fmt)
     assert_gemm_close(out.float().cpu().numpy(), ref, an, wn, f"narrow {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fmt", [0, 2])
+def test_gemm_parity_persistent_many_tiles(cuda_lib, orc, fmt):
+    """More 256-wide tiles than SMs, so one persistent CTA per SM walks
+    several tiles: 16 row tiles (the last one ragged) x 32 column tiles;
+    three sampled rows of every row tile against the oracle."""
+    bfq = cuda_lib
+    M, N, K = 2000, 8192, 256
+    assert bfq.bfq_gemm_workspace_bytes(M, N, K) == 0
+    aq, sa, wq, sw = _oracle_problem(orc, M, N, K, fmt, seed=31 + fmt)
+    d = _to_dev(aq, sa, wq, sw, fmt)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bfq.gemm(d[0], d[1], fmt, d[2], d[3], out=out)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(fmt)
+    rows = np.unique(np.concatenate(
+        [[t * 128, min(M, t * 128 + 128) - 1, rng.integers(t * 128, min(M, t * 128 + 128))]
+         for t in range((M + 127) // 128)]))
+    ref = orc.gemm(aq, sa, fmt, wq, sw, rows=rows)
+    an, wn = _norms(orc, aq, sa, wq, sw, fmt, rows=rows)
+    got = out.float().cpu().numpy()
+    assert_gemm_close(got[rows], ref, an, wn, f"persistent {M}x{N}x{K} fmt{fmt}")
+    assert np.isfinite(got).all()

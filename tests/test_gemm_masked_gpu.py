@@ -141,3 +141,16 @@ def test_moe_expert_slice_chain(cuda_lib, orc):
         wn = np.linalg.norm(orc.dequant_weight(dq, dsw), axis=1)
         err = np.abs(oh[e, :c] - ref) / (an[:, None] * wn[None, :])
         assert np.isfinite(oh[e, :c]).all() and err.max() <= 2e-3, (e, float(err.max()))
+
+
+def test_masked_gemm_more_tiles_than_sms(cuda_lib, orc):
+    """16 experts with counts from 0 to 256 over 10 column tiles: 210 valid
+    tiles, more than one per SM, so the persistent schedule walks several
+    per CTA.  Every expert's padded rows stay untouched; first, middle and
+    last valid rows of every non-empty expert match the oracle."""
+    E, T, N, K = 16, 256, 2560, 256
+    cnt = np.array([0, 1, 127, 128, 129, 256, 255, 64, 200, 0, 17, 256, 130, 90, 3, 240],
+                   np.int32)
+    experts = {e for e in range(E) if cnt[e] > 0}
+    aq, sa, wq, sw, _ = _expert_problem(orc, E, T, N, K, cnt, 2, seed=123, experts=experts)
+    _run_and_check(cuda_lib, orc, aq, sa, wq, sw, cnt, 2, experts=experts)
