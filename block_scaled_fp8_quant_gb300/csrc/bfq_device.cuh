@@ -345,56 +345,10 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per
-// thread), followed by the wait for the load to land in registers.  Load
-// and wait are one asm statement so no use of the registers can be
-// scheduled before the data is valid.
-__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes delivered as 16
-// register pairs (column 2i in the low half of p[i]), followed by the wait
-// for the load — one asm statement, so no use can precede the data.
-__device__ __forceinline__ void tmem_ld32_pairs_wait(uint32_t taddr, uint64_t (&p)[16]) {
-  asm volatile(
-      "{\n\t.reg .b32 t<32>;\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,"
-      "t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;\n\t"
-      "mov.b64 %0, {t0,t1};\n\tmov.b64 %1, {t2,t3};\n\t"
-      "mov.b64 %2, {t4,t5};\n\tmov.b64 %3, {t6,t7};\n\t"
-      "mov.b64 %4, {t8,t9};\n\tmov.b64 %5, {t10,t11};\n\t"
-      "mov.b64 %6, {t12,t13};\n\tmov.b64 %7, {t14,t15};\n\t"
-      "mov.b64 %8, {t16,t17};\n\tmov.b64 %9, {t18,t19};\n\t"
-      "mov.b64 %10, {t20,t21};\n\tmov.b64 %11, {t22,t23};\n\t"
-      "mov.b64 %12, {t24,t25};\n\tmov.b64 %13, {t26,t27};\n\t"
-      "mov.b64 %14, {t28,t29};\n\tmov.b64 %15, {t30,t31};\n\t}\n"
-      : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]),
-        "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]),
-        "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
-      : "r"(taddr)
-      : "memory");
-}
-
-// 64 consecutive fp32 columns of this warp's 32 TMEM lanes as 32 register
-// pairs (column 2i in the low half of p[i]), load and wait in one statement.
+// 64 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per
+// thread) as 32 register pairs (column 2i in the low half of p[i]).  Load and
+// wait are one asm statement, so no use of the registers can be scheduled
+// before the data is valid.
 __device__ __forceinline__ void tmem_ld64_pairs_wait(uint32_t taddr, uint64_t (&p)[32]) {
   asm volatile(
       "{\n\t.reg .b32 t<64>;\n\t"

@@ -42,27 +42,18 @@ constexpr int kMaxSplits = 8;  // K splits of a tile form one (portable-size) cl
 // the allocation the kernel is launched with (checked on the host).
 // Warp 2 streams the scales into shared memory.  BN = 128: seven warps, two
 // per sub-partition at most, no reconfiguration.
-// BN = 128 with MINB = 2 ("paired"): two CTAs share an SM so that one CTA's
-// set-up, pipeline fill and epilogue overlap the other's main loop.  Each
-// holds half the SM's registers, TMEM and shared memory: two warpgroups
-// (warpgroup 0 at 24 registers, the four epilogue warps at 232:
-// 128*24 + 128*232 = 32768 = 256 threads * 128), a 3-stage ring (~102 KB)
-// and 256 TMEM columns; the epilogue reads TMEM 32 columns at a time.
-template <int BN, int MINB = 1>
+template <int BN>
 struct GemmCfg {
-  static constexpr bool kPaired = (MINB == 2);
-  static_assert(MINB == 1 || (MINB == 2 && BN == 128), "two CTAs per SM only with BN = 128");
-  static constexpr int kStages = (BN == 256) ? 4 : (kPaired ? 3 : 6);
+  static constexpr int kStages = (BN == 256) ? 4 : 6;
   static constexpr int kEpiWarps = BN / 32;  // 128 columns per warp
-  static constexpr int kEpiWarp0 = (BN == 256 || kPaired) ? 4 : 3;
+  static constexpr int kEpiWarp0 = (BN == 256) ? 4 : 3;
   static constexpr int kScaleWarp = 2;       // streams the scales into smem
   static constexpr int kScaleSlots = 8;      // K blocks of scales in flight
   static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
-  static constexpr bool kRegSplit = (BN == 256) || kPaired;
-  static constexpr int kLaunchRegs = kPaired ? 128 : 168;
+  static constexpr bool kRegSplit = (BN == 256);
+  static constexpr int kLaunchRegs = 168;
   static constexpr int kProducerRegs = 24;
-  static constexpr int kEpilogueRegs = kPaired ? 232 : 240;
-  static constexpr int kLdCols = kPaired ? 32 : 64;  // TMEM columns per tcgen05.ld
+  static constexpr int kEpilogueRegs = 240;
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -97,12 +88,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int BN, bool MASKED, int MINB = 1>
-__global__ void __launch_bounds__(GemmCfg<BN, MINB>::kThreads, MINB)
+template <int BN, bool MASKED>
+__global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
     gemm_block_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmW,
                           const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
-  using C = GemmCfg<BN, MINB>;
+  using C = GemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
@@ -307,22 +298,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, MINB>::kThreads, MINB)
       if (warp_active) {
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                (uint32_t)(buf * BN + half * 128);
-        if constexpr (C::kLdCols == 64) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint64_t v[32];
-            tmem_ld64_pairs_wait(taddr + (uint32_t)(h * 64), v);
+        for (int h = 0; h < 2; ++h) {
+          uint64_t v[32];
+          tmem_ld64_pairs_wait(taddr + (uint32_t)(h * 64), v);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) ffma2(acc[h * 32 + t], v[t], s2);
-          }
-        } else {
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            uint64_t v[16];
-            tmem_ld32_pairs_wait(taddr + (uint32_t)(h * 32), v);
-#pragma unroll
-            for (int t = 0; t < 16; ++t) ffma2(acc[h * 16 + t], v[t], s2);
-          }
+          for (int t = 0; t < 32; ++t) ffma2(acc[h * 32 + t], v[t], s2);
         }
       }
       tc_fence_before_sync();
@@ -870,7 +851,6 @@ bool make_out_map(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows) {
 
 struct Plan {
   int bn = 256;
-  int minb = 1;          // CTAs per SM (2: the paired 128-wide configuration)
   bool persist = false;  // persistent 256-wide kernel (no K split)
   int m_tiles = 0, n_tiles = 0, splits = 1;
   size_t ws_bytes = 0;  // bytes needed by this plan
@@ -935,9 +915,9 @@ Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, size_t w
   return pl;
 }
 
-template <int BN, bool MASKED, int MINB = 1>
+template <int BN, bool MASKED>
 bfq_status configure(const DeviceInfo& dev) {
-  using C = GemmCfg<BN, MINB>;
+  using C = GemmCfg<BN>;
   static bool configured[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
@@ -946,21 +926,15 @@ bfq_status configure(const DeviceInfo& dev) {
     // setmaxnreg.inc only completes if the launch allocation covers the
     // split; refuse to launch a build whose register count differs.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, gemm_block_fp8_kernel<BN, MASKED, MINB>) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, gemm_block_fp8_kernel<BN, MASKED>) != cudaSuccess) {
       cudaGetLastError();
       return BFQ_ERR_CUDA;
     }
     if (fa.numRegs != C::kLaunchRegs) return BFQ_ERR_DEVICE;
   }
-  if (cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED, MINB>,
+  if (cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)C::kSmemBytes) != cudaSuccess) {
-    cudaGetLastError();
-    return BFQ_ERR_CUDA;
-  }
-  if (C::kPaired && cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED, MINB>,
-                                         cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
     cudaGetLastError();
     return BFQ_ERR_CUDA;
   }
@@ -1003,13 +977,13 @@ int max_active_clusters(const DeviceInfo& dev, int cluster) {
   return n;
 }
 
-template <int BN, bool MASKED, int MINB = 1>
+template <int BN, bool MASKED>
 bfq_status launch(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
                   const CUtensorMap& mo, const GemmParams& p, unsigned grid, cudaStream_t s) {
-  using C = GemmCfg<BN, MINB>;
-  bfq_status st = configure<BN, MASKED, MINB>(dev);
+  using C = GemmCfg<BN>;
+  bfq_status st = configure<BN, MASKED>(dev);
   if (st != BFQ_OK) return st;
-  return launch_status(launch_pdl(gemm_block_fp8_kernel<BN, MASKED, MINB>, dim3(grid),
+  return launch_status(launch_pdl(gemm_block_fp8_kernel<BN, MASKED>, dim3(grid),
                                   dim3(C::kThreads), C::kSmemBytes, s,
                                   p.splits > 1 ? (unsigned)p.splits : 1u, ma, mw, mo, p));
 }
@@ -1124,8 +1098,7 @@ extern "C" bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, 
   if (pl.persist)
     return launch_persistent<false>(dev, ma, mw, mo, p, grid < (unsigned)dev.sm_count
                                                            ? grid : (unsigned)dev.sm_count, s);
-  if (pl.bn == 256) return launch<256, false>(dev, ma, mw, mo, p, grid, s);
-  return pl.minb == 2 ? launch<128, false, 2>(dev, ma, mw, mo, p, grid, s)
+  return pl.bn == 256 ? launch<256, false>(dev, ma, mw, mo, p, grid, s)
                       : launch<128, false>(dev, ma, mw, mo, p, grid, s);
 }
 
@@ -1182,9 +1155,8 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked(
   if (mp.persist)
     return launch_persistent<true>(dev, ma, mw, mw, p,
                                    (unsigned)(grid < dev.sm_count ? grid : dev.sm_count), s);
-  if (bn == 256) return launch<256, true>(dev, ma, mw, mw, p, (unsigned)grid, s);
-  return mp.minb == 2 ? launch<128, true, 2>(dev, ma, mw, mw, p, (unsigned)grid, s)
-                      : launch<128, true>(dev, ma, mw, mw, p, (unsigned)grid, s);
+  return bn == 256 ? launch<256, true>(dev, ma, mw, mw, p, (unsigned)grid, s)
+                   : launch<128, true>(dev, ma, mw, mw, p, (unsigned)grid, s);
 }
 
 // ----------------------------------------------------------------------------
