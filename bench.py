@@ -523,6 +523,7 @@ def run_gpu(args, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     fp8_peak = float(peaks["bf16_tflops"]) * FP8_PER_BF16
+    fp8_peak_sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * FP8_PER_BF16
 
     if args.moe_only:  # profiling mode: the MoE expert slice only, no report
         measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, 2)
@@ -663,7 +664,9 @@ def run_gpu(args, rank, world, local_rank):
                      "peak_source": f"{peak_src} bf16 burst x {FP8_PER_BF16} (fp8:bf16 nominal)",
                      "alg_bytes_per_launch_avg": gemm_bytes_avg,
                      "avg_launch_us": round(gemm_launch_ms * 1e3, 2),
-                     "mixed_frac": round(t_roof_sum * 1e3 / (gemm_ms_total / reps), 4)},
+                     "mixed_frac": round(t_roof_sum * 1e3 / (gemm_ms_total / reps), 4),
+                     "peak_sustained": fp8_peak_sustained,
+                     "frac_of_sustained": round(achieved_tflops / fp8_peak_sustained, 4)},
         "quant": {"total_us_per_step": round(quant_ms_total / reps * 1e3, 1),
                   "hbm_peak_gbs": hbm_peak},
         "clocks": clk.summary(),

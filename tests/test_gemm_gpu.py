@@ -163,13 +163,13 @@ def test_gemm_parity_narrow_unsplit_plan(cuda_lib, orc, fmt, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", [0, 2])
-@pytest.mark.parametrize("M,N,K", [(2000, 8192, 256), (2048, 2432, 256)])
+@pytest.mark.parametrize("M,N,K", [(2000, 8192, 256), (2048, 2432, 256), (1100, 5120, 256)])
 def test_gemm_parity_persistent_many_tiles(cuda_lib, orc, fmt, M, N, K):
-    """More 256-wide tiles than SMs, so one persistent CTA per SM walks
-    several tiles.  2000 x 8192: 16 row tiles (the last one ragged) x 32
-    column tiles, 512 tiles, the last 56 run as 128-wide halves; 2048 x 2432:
-    the last column tile half full (no halves).  Three sampled rows of every
-    row tile against the oracle, every column."""
+    """More 256-wide tiles than SMs, so the persistent schedule walks several
+    tiles per SM.  2000 x 8192: 16 row tiles, the last one ragged, x 32
+    column tiles; 2048 x 2432: the last column tile half full; 1100 x 5120:
+    an odd number of row tiles.  Three sampled rows of every row tile against
+    the oracle, every column."""
     bfq = cuda_lib
     assert bfq.bfq_gemm_workspace_bytes(M, N, K) == 0
     aq, sa, wq, sw = _oracle_problem(orc, M, N, K, fmt, seed=31 + fmt + N)
