@@ -660,7 +660,7 @@ def run_gpu(args, rank, world, local_rank):
                      "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": round(achieved_tflops / fp8_peak, 4),
                      "traffic": traffic,
-                     "kernel": "gemm_block_fp8_kernel (all 36 sweep launches)",
+                     "kernel": "block-FP8 GEMM: gemm_block_fp8_kernel and gemm_block_fp8_persistent (all 36 sweep launches)",
                      "peak_source": f"{peak_src} bf16 burst x {FP8_PER_BF16} (fp8:bf16 nominal)",
                      "alg_bytes_per_launch_avg": gemm_bytes_avg,
                      "avg_launch_us": round(gemm_launch_ms * 1e3, 2),
