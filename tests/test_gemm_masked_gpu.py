@@ -154,3 +154,18 @@ def test_masked_gemm_more_tiles_than_sms(cuda_lib, orc):
     experts = {e for e in range(E) if cnt[e] > 0}
     aq, sa, wq, sw, _ = _expert_problem(orc, E, T, N, K, cnt, 2, seed=123, experts=experts)
     _run_and_check(cuda_lib, orc, aq, sa, wq, sw, cnt, 2, experts=experts)
+
+
+@pytest.mark.parametrize("E,T,N,K,fmt", [(3, 136, 128, 256, 0), (1100, 16, 256, 128, 2)])
+def test_masked_gemm_per_tile_forms(cuda_lib, orc, E, T, N, K, fmt):
+    """The per-tile masked kernel: 128-wide tiles (N <= 128), and more experts
+    than the persistent schedule's prefix table holds (E > 1024).  Padded
+    rows of every expert stay untouched; sampled rows of a spread of experts
+    match the oracle."""
+    rng = np.random.default_rng(E + N)
+    cnt = rng.integers(0, T + 1, E).astype(np.int32)
+    cnt[0], cnt[-1] = 0, T
+    nz = [e for e in range(E) if cnt[e] > 0]
+    experts = set(nz[:: max(1, len(nz) // 6)]) | {nz[-1]}
+    aq, sa, wq, sw, _ = _expert_problem(orc, E, T, N, K, cnt, fmt, seed=E + T, experts=experts)
+    _run_and_check(cuda_lib, orc, aq, sa, wq, sw, cnt, fmt, experts=experts)
