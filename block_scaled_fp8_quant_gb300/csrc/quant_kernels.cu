@@ -35,17 +35,28 @@ __device__ __forceinline__ float quant16(const float (&v)[16], uint4& codes) {
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
   float s = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
   uint32_t c[8];
+  // The quotients are formed two at a time with packed f32x2 operations; each
+  // lane of a pair is rounded exactly as the scalar operation, so the codes
+  // are those of group_div (fp32 scales) and of one multiply (powers of two).
   if (FMT == BFQ_SCALE_F32) {
     const float y = __frcp_rn(s);
+    const uint64_t y2 = splat2(y), neg_s2 = splat2(-s);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      c[i] = cvt_e4m3x2(group_div(v[2 * i], s, y), group_div(v[2 * i + 1], s, y));
+    for (int i = 0; i < 8; ++i) {
+      const uint64_t a = pack2(v[2 * i], v[2 * i + 1]);
+      const uint64_t q0 = mul2_rn(a, y2);
+      const uint64_t r = fma2_rn(q0, neg_s2, a);  // fma(-q0, s, a), exactly
+      const float2 q = unpack2(fma2_rn(r, y2, q0));
+      c[i] = cvt_e4m3x2(copysignf(q.x, v[2 * i]), copysignf(q.y, v[2 * i + 1]));
+    }
   } else {
     s = ceil_pow2(s);
-    const float y = __frcp_rn(s);  // exact: s is a power of two
+    const uint64_t y2 = splat2(__frcp_rn(s));  // exact: s is a power of two
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      c[i] = cvt_e4m3x2(__fmul_rn(v[2 * i], y), __fmul_rn(v[2 * i + 1], y));
+    for (int i = 0; i < 8; ++i) {
+      const float2 q = unpack2(mul2_rn(pack2(v[2 * i], v[2 * i + 1]), y2));
+      c[i] = cvt_e4m3x2(q.x, q.y);
+    }
   }
   codes.x = c[0] | (c[1] << 16);
   codes.y = c[2] | (c[3] << 16);
