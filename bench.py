@@ -506,8 +506,17 @@ def measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, reps):
     us = gated_times(torch, act, reps)
     nbytes = tot * (2 * I * 2 + I) + tot * (I // 512) * 4
     gbs = nbytes / (us * 1e-6) / 1e9
+    # back to back over rotating inputs (4 x 64 MB, more than twice the L2)
+    hs = [h] + [synth.masked_activation(E, T, 2 * I, counts, seed=950 + c, device=dev)
+                for c in range(3)]
+    us_b2b = graph_back_to_back_us(
+        torch, lambda i: bfq.bfq_silu_mul_quant(hs[i], d_counts, a_dn, sa_dn, 2, T), len(hs), 16)
+    gbs_b2b = nbytes / (us_b2b * 1e-6) / 1e9
     res["silu_mul_quant"] = {"us": round(us, 2), "gbps": round(gbs, 1),
-                             "hbm_frac": round(gbs / hbm_peak, 3), "bytes": nbytes}
+                             "hbm_frac": round(gbs / hbm_peak, 3), "us_b2b": round(us_b2b, 2),
+                             "gbps_b2b": round(gbs_b2b, 1),
+                             "hbm_frac_b2b": round(gbs_b2b / hbm_peak, 3), "bytes": nbytes}
+    del hs
     del w_up, w_dn, x, h
     return res
 
