@@ -81,6 +81,13 @@ struct GemmParams {
   int m_tiles, n_tiles, splits;
   int a_fmt;
   int E;                   // masked: experts
+  // fused output quant (QOUT kernels): the bf16-rounded output quantized per
+  // 1 x 128 group into q_out (e4m3 [M][N]) and q_scales (format q_fmt,
+  // column-major, leading dimension q_scale_ld); out may then be null.
+  uint8_t* q_out;
+  void* q_scales;
+  int64_t q_scale_ld;
+  int q_fmt;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -88,7 +95,60 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int BN, bool MASKED>
+// Fused output quant of one row's 128 accumulated columns, which form exactly
+// one 1 x 128 group (the tile's column halves start at multiples of 128): the
+// values are rounded to bf16 as the output is stored, then quantized as the
+// per-token-group quant kernel quantizes a bf16 input — group amax, scale
+// fl32(max(amax, eps) / 448) (power of two for the pow2 and UE8M0 formats),
+// correctly rounded quotient, saturating e4m3 — so the codes and scales are
+// those of quantizing the stored bf16 output ("[Perf] Deepgemm fused layout
+// kernel for activations": no separate quant or layout pass).
+//   q_row   &q_out[m][col0];  group = col0 / 128;  last = this is the row's
+//   last group (a packed word it leaves incomplete gets zero bytes).
+__device__ __forceinline__ void quant_store_row_group(const uint64_t (&acc)[64], uint8_t* q_row,
+                                                      void* scales, int64_t ld, int m, int group,
+                                                      bool last, int fmt) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    const float2 f = unpack2(acc[j]);
+    const uint32_t b = pack_bf16x2(f.x, f.y);
+    amax = fmaxf(amax, fmaxf(fabsf(bf16lo(b)), fabsf(bf16hi(b))));
+  }
+  float s = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
+  if (fmt != BFQ_SCALE_F32) s = ceil_pow2(s);
+  const float y = __frcp_rn(s);  // exact for a power of two
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // 16 codes per 16-byte store
+    uint32_t w[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 f0 = unpack2(acc[c * 8 + 2 * t]), f1 = unpack2(acc[c * 8 + 2 * t + 1]);
+      const uint32_t b0 = pack_bf16x2(f0.x, f0.y), b1 = pack_bf16x2(f1.x, f1.y);
+      const float v0 = bf16lo(b0), v1 = bf16hi(b0), v2 = bf16lo(b1), v3 = bf16hi(b1);
+      uint32_t lo, hi;
+      if (fmt == BFQ_SCALE_F32) {
+        lo = cvt_e4m3x2(group_div(v0, s, y), group_div(v1, s, y));
+        hi = cvt_e4m3x2(group_div(v2, s, y), group_div(v3, s, y));
+      } else {
+        lo = cvt_e4m3x2(__fmul_rn(v0, y), __fmul_rn(v1, y));
+        hi = cvt_e4m3x2(__fmul_rn(v2, y), __fmul_rn(v3, y));
+      }
+      w[t] = lo | (hi << 16);
+    }
+    st_v4(q_row + c * 16, make_uint4(w[0], w[1], w[2], w[3]));
+  }
+  if (fmt == BFQ_SCALE_UE8M0_PACKED) {
+    uint8_t* word = (uint8_t*)scales + ((int64_t)(group >> 2) * ld + m) * 4;
+    word[group & 3] = (uint8_t)ue8m0_byte(s);
+    if (last)
+      for (int b = (group & 3) + 1; b < 4; ++b) word[b] = 0;
+  } else {
+    ((float*)scales)[(int64_t)group * ld + m] = s;
+  }
+}
+
+template <int BN, bool MASKED, bool QOUT = false>
 __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
     gemm_block_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmW,
@@ -314,34 +374,43 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
     const bool ok = !*abort_flag;
     const int64_t out_row = (MASKED ? (int64_t)e * p.out_estride : 0) + (int64_t)m * p.N;
     if (p.splits == 1 && !MASKED) {
-      // Dense tile: stage the bf16 tile in the (now idle) A stages as
-      // [BN/64] boxes of 128 rows x 64 columns in the 128-byte swizzled layout
-      // (16-byte chunk c of row r at chunk c ^ (r mod 8): conflict-free), then
-      // one thread writes them with TMA stores, which clip rows >= M.
-      if (ok && warp_active) {
+      // (fused output quant: the bf16 output is optional)
+      if (!QOUT || p.out != nullptr) {
+        // Dense tile: stage the bf16 tile in the (now idle) A stages as
+        // [BN/64] boxes of 128 rows x 64 columns in the 128-byte swizzled layout
+        // (16-byte chunk c of row r at chunk c ^ (r mod 8): conflict-free), then
+        // one thread writes them with TMA stores, which clip rows >= M.
+        if (ok && warp_active) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int blk = half * 2 + j;
-          if (j * 64 >= ncols) break;  // this 64-column block lies beyond N
-          const uint32_t row_addr =
-              smem_u32(smem) + (uint32_t)(blk * (kBM * 128) + row_local * 128);
+          for (int j = 0; j < 2; ++j) {
+            const int blk = half * 2 + j;
+            if (j * 64 >= ncols) break;  // this 64-column block lies beyond N
+            const uint32_t row_addr =
+                smem_u32(smem) + (uint32_t)(blk * (kBM * 128) + row_local * 128);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int a = j * 32 + c * 4;  // pair index of column j*64 + c*8
-            const float2 f0 = unpack2(acc[a + 0]), f1 = unpack2(acc[a + 1]);
-            const float2 f2 = unpack2(acc[a + 2]), f3 = unpack2(acc[a + 3]);
-            st_shared_v4(row_addr + (uint32_t)((c ^ (row_local & 7)) << 4),
-                         make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
-                                    pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
+            for (int c = 0; c < 8; ++c) {
+              const int a = j * 32 + c * 4;  // pair index of column j*64 + c*8
+              const float2 f0 = unpack2(acc[a + 0]), f1 = unpack2(acc[a + 1]);
+              const float2 f2 = unpack2(acc[a + 2]), f3 = unpack2(acc[a + 3]);
+              st_shared_v4(row_addr + (uint32_t)((c ^ (row_local & 7)) << 4),
+                           make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
+                                      pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
+            }
           }
         }
+        fence_proxy_async_smem();
+        named_barrier(1, C::kEpiWarps * 32);
+        if (threadIdx.x == C::kEpiWarp0 * 32 && !*abort_flag) {
+          for (int blk = 0; blk < BN / 64; ++blk)
+            if (n0 + blk * 64 < p.N)
+              tma_store_2d(&tmO, smem + blk * (kBM * 128), n0 + blk * 64, m0);
+          bulk_commit_and_wait_all();
+        }
       }
-      fence_proxy_async_smem();
-      named_barrier(1, C::kEpiWarps * 32);
-      if (threadIdx.x == C::kEpiWarp0 * 32 && !*abort_flag) {
-        for (int blk = 0; blk < BN / 64; ++blk)
-          if (n0 + blk * 64 < p.N) tma_store_2d(&tmO, smem + blk * (kBM * 128), n0 + blk * 64, m0);
-        bulk_commit_and_wait_all();
+      if constexpr (QOUT) {
+        if (ok && warp_active && row_ok)
+          quant_store_row_group(acc, p.q_out + (int64_t)m * p.N + col0, p.q_scales, p.q_scale_ld,
+                                m, col0 >> 7, col0 + 128 >= p.N, p.q_fmt);
       }
     } else if (p.splits == 1) {
       if (ok && warp_active && row_ok) {
@@ -470,7 +539,7 @@ __device__ __forceinline__ void persist_tile(int t, const GemmParams& p, const i
   }
 }
 
-template <bool MASKED>
+template <bool MASKED, bool QOUT = false>
 __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
     gemm_block_fp8_persistent(const __grid_constant__ CUtensorMap tmA,
                               const __grid_constant__ CUtensorMap tmW,
@@ -566,7 +635,8 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
   // Tiles of this CTA and the K blocks they stream, as one flat sequence
   // g = 0 .. steps-1 (tile g / KB, K block g mod KB): the warps that run at
   // 24 registers keep only a counter and the current tile's coordinates.
-  const int my_tiles = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int my_tiles =
+      (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int steps = my_tiles * KB;
   static_assert((C::kStages & (C::kStages - 1)) == 0 && C::kStages == 4, "ring of 4 stages");
   static_assert(C::kScaleSlots == 8, "scale ring of 8 slots");
@@ -757,9 +827,10 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
       } else {
         // Four 128 x 64 boxes through the staging buffer (128-byte swizzle,
         // 16-byte chunk c of row r at chunk c ^ (r mod 8)); rows >= M are
-        // clipped by the tensor map.
+        // clipped by the tensor map.  (Fused output quant: the bf16 output is
+        // optional; the condition is the same for every thread.)
 #pragma unroll
-        for (int blk = 0; blk < BN / 64; ++blk) {
+        for (int blk = 0; blk < ((!QOUT || p.out != nullptr) ? BN / 64 : 0); ++blk) {
           if (store_thread) bulk_wait_read_all();  // previous box has left the buffer
           named_barrier(1, C::kEpiWarps * 32);
           if (half == (blk >> 1) && warp_active) {
@@ -780,6 +851,11 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
             tma_store_2d(&tmO, stg, n0 + blk * 64, m0);
             bulk_commit();
           }
+        }
+        if constexpr (QOUT) {
+          if (warp_active && row_ok)
+            quant_store_row_group(acc, p.q_out + (int64_t)m * p.N + col0, p.q_scales,
+                                  p.q_scale_ld, m, col0 >> 7, col0 + 128 >= p.N, p.q_fmt);
         }
       }
     }
@@ -915,7 +991,7 @@ Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, size_t w
   return pl;
 }
 
-template <int BN, bool MASKED>
+template <int BN, bool MASKED, bool QOUT = false>
 bfq_status configure(const DeviceInfo& dev) {
   using C = GemmCfg<BN>;
   static bool configured[64] = {};
@@ -926,13 +1002,13 @@ bfq_status configure(const DeviceInfo& dev) {
     // setmaxnreg.inc only completes if the launch allocation covers the
     // split; refuse to launch a build whose register count differs.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, gemm_block_fp8_kernel<BN, MASKED>) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, gemm_block_fp8_kernel<BN, MASKED, QOUT>) != cudaSuccess) {
       cudaGetLastError();
       return BFQ_ERR_CUDA;
     }
     if (fa.numRegs != C::kLaunchRegs) return BFQ_ERR_DEVICE;
   }
-  if (cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED>,
+  if (cudaFuncSetAttribute(gemm_block_fp8_kernel<BN, MASKED, QOUT>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)C::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
@@ -977,13 +1053,13 @@ int max_active_clusters(const DeviceInfo& dev, int cluster) {
   return n;
 }
 
-template <int BN, bool MASKED>
+template <int BN, bool MASKED, bool QOUT = false>
 bfq_status launch(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
                   const CUtensorMap& mo, const GemmParams& p, unsigned grid, cudaStream_t s) {
   using C = GemmCfg<BN>;
-  bfq_status st = configure<BN, MASKED>(dev);
+  bfq_status st = configure<BN, MASKED, QOUT>(dev);
   if (st != BFQ_OK) return st;
-  return launch_status(launch_pdl(gemm_block_fp8_kernel<BN, MASKED>, dim3(grid),
+  return launch_status(launch_pdl(gemm_block_fp8_kernel<BN, MASKED, QOUT>, dim3(grid),
                                   dim3(C::kThreads), C::kSmemBytes, s,
                                   p.splits > 1 ? (unsigned)p.splits : 1u, ma, mw, mo, p));
 }
@@ -999,20 +1075,20 @@ Plan masked_plan(const DeviceInfo& dev, int64_t E, int64_t T, int64_t N, int64_t
   return pl;
 }
 
-template <bool MASKED>
+template <bool MASKED, bool QOUT = false>
 bfq_status configure_persistent(const DeviceInfo& dev) {
   static bool configured[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (configured[dev.ordinal]) return BFQ_OK;
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, gemm_block_fp8_persistent<MASKED>) != cudaSuccess) {
+  if (cudaFuncGetAttributes(&fa, gemm_block_fp8_persistent<MASKED, QOUT>) != cudaSuccess) {
     cudaGetLastError();
     return BFQ_ERR_CUDA;
   }
   // setmaxnreg.inc only completes if the launch allocation covers the split
   if (fa.numRegs != GemmCfg<256>::kLaunchRegs) return BFQ_ERR_DEVICE;
-  if (cudaFuncSetAttribute(gemm_block_fp8_persistent<MASKED>,
+  if (cudaFuncSetAttribute(gemm_block_fp8_persistent<MASKED, QOUT>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)PersistCfg::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
@@ -1022,13 +1098,13 @@ bfq_status configure_persistent(const DeviceInfo& dev) {
   return BFQ_OK;
 }
 
-template <bool MASKED>
+template <bool MASKED, bool QOUT = false>
 bfq_status launch_persistent(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
                              const CUtensorMap& mo, const GemmParams& p, unsigned grid,
                              cudaStream_t s) {
-  bfq_status st = configure_persistent<MASKED>(dev);
+  bfq_status st = configure_persistent<MASKED, QOUT>(dev);
   if (st != BFQ_OK) return st;
-  return launch_status(launch_pdl(gemm_block_fp8_persistent<MASKED>, dim3(grid),
+  return launch_status(launch_pdl(gemm_block_fp8_persistent<MASKED, QOUT>, dim3(grid),
                                   dim3(GemmCfg<256>::kThreads), PersistCfg::kSmemBytes, s, 1u, ma,
                                   mw, mo, p));
 }
@@ -1053,31 +1129,51 @@ extern "C" size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return dense_plan(dev, M, N, K, 0, false).ws_bytes;
 }
 
-extern "C" bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, int32_t a_fmt,
-                                         int64_t a_scale_ld, const void* w_q,
-                                         const float* w_scales, int64_t M, int64_t N,
-                                         int64_t K, void* out, void* workspace,
-                                         size_t workspace_bytes, void* stream) {
+namespace bfq {
+namespace {
+
+// Optional fused output quant of a dense GEMM (null: plain bf16 output).
+struct QuantOut {
+  int32_t fmt;
+  void* q;
+  void* scales;
+  int64_t scale_ld;
+};
+
+bfq_status gemm_dense(const void* a_q, const void* a_scales, int32_t a_fmt, int64_t a_scale_ld,
+                      const void* w_q, const float* w_scales, int64_t M, int64_t N, int64_t K,
+                      void* out, void* workspace, size_t workspace_bytes, const QuantOut* qo,
+                      void* stream) {
   if (M < 0 || N <= 0 || K <= 0 || !valid_fmt(a_fmt) || a_scale_ld < M)
     return BFQ_ERR_INVALID_ARG;
   if (K % 128 != 0 || N % 64 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
   if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (qo) {
+    if (!valid_fmt(qo->fmt) || qo->scale_ld < M) return BFQ_ERR_INVALID_ARG;
+    if (N % 128 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  }
   if (M == 0) return BFQ_OK;
-  if (!a_q || !a_scales || !w_q || !w_scales || !out) return BFQ_ERR_INVALID_ARG;
-  if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(out) || a_scale_ld % 4 != 0 ||
+  if (!a_q || !a_scales || !w_q || !w_scales || (!out && !qo)) return BFQ_ERR_INVALID_ARG;
+  if (qo && (!qo->q || !qo->scales)) return BFQ_ERR_INVALID_ARG;
+  if (!aligned16(a_q) || !aligned16(w_q) || (out && !aligned16(out)) || a_scale_ld % 4 != 0 ||
       ((uintptr_t)a_scales & 3u) || ((uintptr_t)w_scales & 3u))
+    return BFQ_ERR_MISALIGNED;
+  if (qo && (!aligned16(qo->q) || ((uintptr_t)qo->scales & 3u) || qo->scale_ld % 4 != 0))
     return BFQ_ERR_MISALIGNED;
   if (workspace_bytes > 0 && !workspace) return BFQ_ERR_INVALID_ARG;
   if (workspace && !aligned16(workspace)) return BFQ_ERR_MISALIGNED;
   DeviceInfo dev;
   bfq_status st = check_device(&dev);
   if (st != BFQ_OK) return st;
-  Plan pl = dense_plan(dev, M, N, K, workspace ? workspace_bytes : 0, true);
+  // The fused quant needs whole output rows per thread: no K split.
+  Plan pl = qo ? dense_plan(dev, M, N, K, 0, true)
+               : dense_plan(dev, M, N, K, workspace ? workspace_bytes : 0, true);
   CUtensorMap ma, mw, mo;
   if (!make_map(&ma, a_q, (uint64_t)K, (uint64_t)M, kBM) ||
-      !make_map(&mw, w_q, (uint64_t)K, (uint64_t)N, (uint32_t)pl.bn) ||
-      !make_out_map(&mo, out, (uint64_t)N, (uint64_t)M))
+      !make_map(&mw, w_q, (uint64_t)K, (uint64_t)N, (uint32_t)pl.bn))
     return BFQ_ERR_CUDA;
+  if (out ? !make_out_map(&mo, out, (uint64_t)N, (uint64_t)M) : false) return BFQ_ERR_CUDA;
+  if (!out) mo = ma;  // never used: the kernels skip the bf16 store
   GemmParams p{};
   p.sa = a_scales;
   p.sa_ld = a_scale_ld;
@@ -1092,14 +1188,47 @@ extern "C" bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, 
   p.n_tiles = pl.n_tiles;
   p.splits = pl.splits;
   p.a_fmt = a_fmt;
+  if (qo) {
+    p.q_out = (uint8_t*)qo->q;
+    p.q_scales = qo->scales;
+    p.q_scale_ld = qo->scale_ld;
+    p.q_fmt = qo->fmt;
+  }
   if (pl.splits > 1) p.ws = (float*)workspace;
   const unsigned grid = (unsigned)(pl.m_tiles * pl.n_tiles * pl.splits);
+  const unsigned pgrid = grid < (unsigned)dev.sm_count ? grid : (unsigned)dev.sm_count;
   cudaStream_t s = (cudaStream_t)stream;
-  if (pl.persist)
-    return launch_persistent<false>(dev, ma, mw, mo, p, grid < (unsigned)dev.sm_count
-                                                           ? grid : (unsigned)dev.sm_count, s);
+  if (qo) {
+    if (pl.persist) return launch_persistent<false, true>(dev, ma, mw, mo, p, pgrid, s);
+    return pl.bn == 256 ? launch<256, false, true>(dev, ma, mw, mo, p, grid, s)
+                        : launch<128, false, true>(dev, ma, mw, mo, p, grid, s);
+  }
+  if (pl.persist) return launch_persistent<false>(dev, ma, mw, mo, p, pgrid, s);
   return pl.bn == 256 ? launch<256, false>(dev, ma, mw, mo, p, grid, s)
                       : launch<128, false>(dev, ma, mw, mo, p, grid, s);
+}
+
+}  // namespace
+}  // namespace bfq
+
+extern "C" bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, int32_t a_fmt,
+                                         int64_t a_scale_ld, const void* w_q,
+                                         const float* w_scales, int64_t M, int64_t N,
+                                         int64_t K, void* out, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  return gemm_dense(a_q, a_scales, a_fmt, a_scale_ld, w_q, w_scales, M, N, K, out, workspace,
+                    workspace_bytes, nullptr, stream);
+}
+
+extern "C" bfq_status bfq_gemm_block_fp8_quant(const void* a_q, const void* a_scales,
+                                               int32_t a_fmt, int64_t a_scale_ld,
+                                               const void* w_q, const float* w_scales, int64_t M,
+                                               int64_t N, int64_t K, void* out, int32_t q_fmt,
+                                               void* q_out, void* q_scales, int64_t q_scale_ld,
+                                               void* stream) {
+  const QuantOut qo{q_fmt, q_out, q_scales, q_scale_ld};
+  return gemm_dense(a_q, a_scales, a_fmt, a_scale_ld, w_q, w_scales, M, N, K, out, nullptr, 0,
+                    &qo, stream);
 }
 
 extern "C" bfq_status bfq_gemm_block_fp8_masked(

@@ -201,6 +201,41 @@ bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, int32_t a_f
                               size_t workspace_bytes, void* stream);
 
 /*
+ * Dense block-scaled FP8 GEMM whose epilogue also quantizes its output for
+ * the next block-FP8 GEMM: the per-token-group (1 x 128) activation quant of
+ * the bf16 result, fused into the GEMM so that the output is not written and
+ * read back before it is quantized (the direction of "[Perf] Deepgemm fused
+ * layout kernel for activations", Purpose: remove an extra kernel and its
+ * memory round trip; [DG-bench] §4.1 for the quant it fuses).
+ *
+ *   C = bf16_rne(GEMM of bfq_gemm_block_fp8)
+ *   q_out, q_scales = bfq_quant(C, group 128, q_fmt, q_scale_ld)
+ *
+ * bit for bit: q_out and q_scales are exactly what bfq_quant writes for the
+ * bf16 output of bfq_gemm_block_fp8 with the same inputs.
+ *
+ *   a_q .. K       as for bfq_gemm_block_fp8, and N % 128 == 0.
+ *   out            bf16 [M][N], or NULL when only the quantized form is
+ *                  wanted.
+ *   q_fmt          scale format of the output quant (any bfq_scale_fmt).
+ *   q_out          e4m3 [M][N], 16-byte aligned.
+ *   q_scales       column-major scales as bfq_quant writes them:
+ *                  float [N/128][q_scale_ld] or uint32 [ceil(N/512)][q_scale_ld]
+ *                  (packed UE8M0, a partial last word with zero bytes for its
+ *                  missing groups); q_scale_ld >= M, q_scale_ld % 4 == 0;
+ *                  columns M .. q_scale_ld-1 are not written.
+ * K is never split (each thread quantizes whole 128-column output groups), so
+ * no workspace is taken; small-m shapes run unsplit.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE (also N % 128 != 0), MISALIGNED,
+ * FORMAT, CUDA, DEVICE.
+ */
+bfq_status bfq_gemm_block_fp8_quant(const void* a_q, const void* a_scales, int32_t a_fmt,
+                                    int64_t a_scale_ld, const void* w_q, const float* w_scales,
+                                    int64_t M, int64_t N, int64_t K, void* out, int32_t q_fmt,
+                                    void* q_out, void* q_scales, int64_t q_scale_ld,
+                                    void* stream);
+
+/*
  * bfq_gemm_block_fp8 for callers that cannot allocate device memory.  (The
  * pages have no counterpart; this is a convenience of this library.)
  *
