@@ -443,6 +443,58 @@ def measure_quant_sweep(bfq, torch, dev, hbm_peak, reps):
     return rows
 
 
+FUSED_SHAPES = [(128, 7168, 18432), (4096, 7168, 18432), (128, 18432, 7168), (4096, 18432, 7168)]
+
+
+def measure_fused_quant(bfq, torch, dev, hbm_peak):
+    """GEMM whose output feeds the next block-FP8 GEMM: the plain GEMM then the
+    1 x 128 quant of its bf16 output (two kernels, the output written and read
+    back) against the GEMM with the quant fused into its epilogue (with and
+    without also writing the bf16 output).  Back-to-back calls over rotating
+    weight copies, fp32 scales in and out."""
+    import bfq_synth as synth
+
+    rows = []
+    for m, n, k in FUSED_SHAPES:
+        copies = max(1, min(4, -(-(300 << 20) // (n * k))))
+        w = synth.weight(n, k, seed=n + k, device=dev)
+        wq0, sw0 = bfq.weight_block_quant(w, bfq.SCALE_F32)
+        del w
+        wqs = [wq0] + [wq0.clone() for _ in range(copies - 1)]
+        sws = [sw0] + [sw0.clone() for _ in range(copies - 1)]
+        x = synth.activation(m, k, seed=m * 31 + n, device=dev)
+        q, s = bfq.quant(x, bfq.SCALE_F32)
+        del x
+        ld = bfq.align4(m)
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        oq = torch.empty((m, n), dtype=torch.float8_e4m3fn, device=dev)
+        osc = torch.empty((n // 128, ld), dtype=torch.float32, device=dev)
+        ws = bfq.gemm_workspace(m, n, k, dev)
+
+        def unfused(i):
+            bfq.bfq_gemm_block_fp8(q, s, 0, s.shape[-1], wqs[i], sws[i], out, ws)
+            bfq.bfq_quant(out, oq, osc, 0, ld)
+
+        def fused(i):
+            bfq.bfq_gemm_block_fp8_quant(q, s, 0, s.shape[-1], wqs[i], sws[i], out, 0, oq, osc, ld,
+                                         workspace=ws)
+
+        def fused_no_out(i):
+            bfq.bfq_gemm_block_fp8_quant(q, s, 0, s.shape[-1], wqs[i], sws[i], None, 0, oq, osc,
+                                         ld, workspace=ws)
+
+        calls = max(2 * copies, 8)
+        t_u = graph_back_to_back_us(torch, unfused, copies, calls)
+        t_f = graph_back_to_back_us(torch, fused, copies, calls)
+        t_fn = graph_back_to_back_us(torch, fused_no_out, copies, calls)
+        rows.append({"m": m, "n": n, "k": k, "unfused_us": round(t_u, 2),
+                     "fused_us": round(t_f, 2), "fused_no_bf16_out_us": round(t_fn, 2),
+                     "saved_frac": round(1.0 - t_f / t_u, 3)})
+        del wqs, sws, q, s, out, oq, osc
+        torch.cuda.empty_cache()
+    return rows
+
+
 def measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, reps):
     """Masked MoE expert slice: up GEMM -> silu-mul-quant -> down GEMM, E=32,
     T_max=256, valid counts ~ U{0..256}, UE8M0 packed activation scales,
@@ -686,6 +738,7 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         line["quant_sweep"] = measure_quant_sweep(bfq, torch, dev, hbm_peak, 10)
         line["moe_slice"] = measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, 10)
+        line["fused_output_quant"] = measure_fused_quant(bfq, torch, dev, hbm_peak)
         if bfq.bfq_poll_device_status() != 0:
             raise RuntimeError("device watchdog fired during the extra measurements")
     if world == 1 and not args.no_cpu_baseline:

@@ -72,7 +72,7 @@ def load_library(build: bool = True):
                                                 I32, P, P, SZ, P]),
             "bfq_gemm_block_fp8_noalloc": (I32, [P, P, I32, I64, P, P, I64, I64, I64, P, P]),
             "bfq_gemm_block_fp8_quant": (I32, [P, P, I32, I64, P, P, I64, I64, I64, P, I32, P, P,
-                                              I64, P]),
+                                              I64, P, SZ, P]),
             "bfq_gemm_noalloc_scratch_bytes": (SZ, []),
             "bfq_poll_device_status": (I32, [P]),
             "bfq_watchdog_selftest": (I32, [I32, P]),
@@ -162,16 +162,19 @@ def bfq_gemm_block_fp8(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w_scales
 
 
 def bfq_gemm_block_fp8_quant(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w_scales, out,
-                             q_fmt: int, q_out, q_scales, q_scale_ld: int, stream=None) -> None:
+                             q_fmt: int, q_out, q_scales, q_scale_ld: int, workspace=None,
+                             stream=None) -> None:
     """GEMM whose epilogue also writes the 1 x 128 group quant of its bf16
     output (out may be None)."""
     lib = load_library()
     M, K = a_q.shape
     N = w_q.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("bfq_gemm_block_fp8_quant",
            lib.bfq_gemm_block_fp8_quant(_ptr(a_q), _ptr(a_scales), a_fmt, a_scale_ld, _ptr(w_q),
                                         _ptr(w_scales), M, N, K, _ptr(out), q_fmt, _ptr(q_out),
-                                        _ptr(q_scales), q_scale_ld, _stream(stream)))
+                                        _ptr(q_scales), q_scale_ld, _ptr(workspace), ws_bytes,
+                                        _stream(stream)))
 
 
 def gemm_quant(a_q, a_scales, a_fmt: int, w_q, w_scales, q_fmt: int, out=None, stream=None):
@@ -183,8 +186,9 @@ def gemm_quant(a_q, a_scales, a_fmt: int, w_q, w_scales, q_fmt: int, out=None, s
     q = torch.empty((M, N), dtype=torch.float8_e4m3fn, device=a_q.device)
     ld = align4(M)
     sc = torch.empty((scale_cols(N, q_fmt), ld), dtype=scale_dtype(q_fmt), device=a_q.device)
+    ws = gemm_workspace(M, N, a_q.shape[1], a_q.device)
     bfq_gemm_block_fp8_quant(a_q, a_scales, a_fmt, a_scales.shape[-1], w_q, w_scales, out, q_fmt,
-                             q, sc, ld, stream=stream)
+                             q, sc, ld, workspace=ws, stream=stream)
     return q, sc
 
 

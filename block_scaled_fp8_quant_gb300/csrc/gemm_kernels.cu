@@ -442,28 +442,104 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
       // summing the partials in split order (deterministic).
       __threadfence();
       cluster_sync();
-      if (!*abort_flag) {
+      // The partials of the next unit are loaded before the current unit is
+      // summed and stored (its stores may alias the loads for the compiler),
+      // so each warp keeps a unit's loads in flight.
+      const float* ws = p.ws;
+      const int64_t plane = (int64_t)p.M * p.N;
+      auto load_parts = [&](int64_t off, float4 (&v)[kMaxSplits]) {
+#pragma unroll
+        for (int t = 0; t < kMaxSplits; ++t)
+          if (t < p.splits) v[t] = __ldcg(reinterpret_cast<const float4*>(ws + t * plane + off));
+      };
+      auto sum_parts = [&](const float4 (&v)[kMaxSplits]) {  // in split order
+        float4 a4 = v[0];
+#pragma unroll
+        for (int t = 1; t < kMaxSplits; ++t)
+          if (t < p.splits) {
+            a4.x += v[t].x; a4.y += v[t].y; a4.z += v[t].z; a4.w += v[t].w;
+          }
+        return a4;
+      };
+      if (QOUT && !*abort_flag) {
+        // Fused output quant: the reduction is shared out in whole 128-column
+        // groups, one warp per (row, group) — 32 lanes x 4 columns — so each
+        // group's amax is one warp reduction.  The sums are formed in split
+        // order exactly as below, so the bf16 output is the same.
+        const int rows = min(kBM, m_limit - m0);
+        const int gpr = min(BN, p.N - n0) / 128;  // output groups per row
+        const int total = rows * gpr;
+        const int u_begin = (int)((int64_t)split * total / p.splits);
+        const int u_end = (int)((int64_t)(split + 1) * total / p.splits);
+        auto unit_off = [&](int u) {
+          const int r = u / gpr;
+          return (int64_t)(m0 + r) * p.N + n0 + (u - r * gpr) * 128 + lane * 4;
+        };
+        float4 vn[kMaxSplits];
+        int u = u_begin + (warp - C::kEpiWarp0);
+        if (u < u_end) load_parts(unit_off(u), vn);
+        for (; u < u_end; u += C::kEpiWarps) {
+          float4 v[kMaxSplits];
+#pragma unroll
+          for (int t = 0; t < kMaxSplits; ++t) v[t] = vn[t];
+          if (u + C::kEpiWarps < u_end) load_parts(unit_off(u + C::kEpiWarps), vn);
+          const int r = u / gpr;
+          const int col = n0 + (u - r * gpr) * 128;
+          const int64_t off = (int64_t)(m0 + r) * p.N + col + lane * 4;
+          const float4 a4 = sum_parts(v);
+          const uint32_t b01 = pack_bf16x2(a4.x, a4.y), b23 = pack_bf16x2(a4.z, a4.w);
+          if (p.out) *reinterpret_cast<uint2*>(p.out + off) = make_uint2(b01, b23);
+          const float x0 = bf16lo(b01), x1 = bf16hi(b01), x2 = bf16lo(b23), x3 = bf16hi(b23);
+          float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+          float sc = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
+          if (p.q_fmt != BFQ_SCALE_F32) sc = ceil_pow2(sc);
+          const float y = __frcp_rn(sc);
+          uint32_t lo, hi;
+          if (p.q_fmt == BFQ_SCALE_F32) {
+            lo = cvt_e4m3x2(group_div(x0, sc, y), group_div(x1, sc, y));
+            hi = cvt_e4m3x2(group_div(x2, sc, y), group_div(x3, sc, y));
+          } else {
+            lo = cvt_e4m3x2(__fmul_rn(x0, y), __fmul_rn(x1, y));
+            hi = cvt_e4m3x2(__fmul_rn(x2, y), __fmul_rn(x3, y));
+          }
+          *reinterpret_cast<uint32_t*>(p.q_out + off) = lo | (hi << 16);
+          if (lane == 0) {
+            const int m = m0 + r, group = col >> 7;
+            if (p.q_fmt == BFQ_SCALE_UE8M0_PACKED) {
+              uint8_t* word =
+                  (uint8_t*)p.q_scales + ((int64_t)(group >> 2) * p.q_scale_ld + m) * 4;
+              word[group & 3] = (uint8_t)ue8m0_byte(sc);
+              if (col + 128 >= p.N)
+                for (int bb = (group & 3) + 1; bb < 4; ++bb) word[bb] = 0;
+            } else {
+              ((float*)p.q_scales)[(int64_t)group * p.q_scale_ld + m] = sc;
+            }
+          }
+        }
+      } else if (!*abort_flag) {
         const int rows = min(kBM, m_limit - m0);
         const int upr = min(BN, p.N - n0) / 4;  // float4 units per row
         const int total = rows * upr;
         const int u_begin = (int)((int64_t)split * total / p.splits);
         const int u_end = (int)((int64_t)(split + 1) * total / p.splits);
-        for (int u = u_begin + (int)threadIdx.x - C::kEpiWarp0 * 32; u < u_end;
-             u += C::kEpiWarps * 32) {
-          const int r = u / upr, c4 = u - (u / upr) * upr;
-          const int64_t off = (int64_t)(m0 + r) * p.N + n0 + c4 * 4;
+        auto unit_off = [&](int u) {
+          const int r = u / upr;
+          return (int64_t)(m0 + r) * p.N + n0 + (u - r * upr) * 4;
+        };
+        constexpr int kStep = C::kEpiWarps * 32;
+        float4 vn[kMaxSplits];
+        int u = u_begin + (int)threadIdx.x - C::kEpiWarp0 * 32;
+        if (u < u_end) load_parts(unit_off(u), vn);
+        for (; u < u_end; u += kStep) {
           float4 v[kMaxSplits];
 #pragma unroll
-          for (int t = 0; t < kMaxSplits; ++t)
-            if (t < p.splits)
-              v[t] = __ldcg(reinterpret_cast<const float4*>(p.ws + (int64_t)t * p.M * p.N + off));
-          float4 a4 = v[0];
-#pragma unroll
-          for (int t = 1; t < kMaxSplits; ++t)
-            if (t < p.splits) {
-              a4.x += v[t].x; a4.y += v[t].y; a4.z += v[t].z; a4.w += v[t].w;
-            }
-          *reinterpret_cast<uint2*>(p.out + off) =
+          for (int t = 0; t < kMaxSplits; ++t) v[t] = vn[t];
+          if (u + kStep < u_end) load_parts(unit_off(u + kStep), vn);
+          const float4 a4 = sum_parts(v);
+          *reinterpret_cast<uint2*>(p.out + unit_off(u)) =
               make_uint2(pack_bf16x2(a4.x, a4.y), pack_bf16x2(a4.z, a4.w));
         }
       }
@@ -1165,9 +1241,7 @@ bfq_status gemm_dense(const void* a_q, const void* a_scales, int32_t a_fmt, int6
   DeviceInfo dev;
   bfq_status st = check_device(&dev);
   if (st != BFQ_OK) return st;
-  // The fused quant needs whole output rows per thread: no K split.
-  Plan pl = qo ? dense_plan(dev, M, N, K, 0, true)
-               : dense_plan(dev, M, N, K, workspace ? workspace_bytes : 0, true);
+  Plan pl = dense_plan(dev, M, N, K, workspace ? workspace_bytes : 0, true);
   CUtensorMap ma, mw, mo;
   if (!make_map(&ma, a_q, (uint64_t)K, (uint64_t)M, kBM) ||
       !make_map(&mw, w_q, (uint64_t)K, (uint64_t)N, (uint32_t)pl.bn))
@@ -1225,10 +1299,11 @@ extern "C" bfq_status bfq_gemm_block_fp8_quant(const void* a_q, const void* a_sc
                                                const void* w_q, const float* w_scales, int64_t M,
                                                int64_t N, int64_t K, void* out, int32_t q_fmt,
                                                void* q_out, void* q_scales, int64_t q_scale_ld,
+                                               void* workspace, size_t workspace_bytes,
                                                void* stream) {
   const QuantOut qo{q_fmt, q_out, q_scales, q_scale_ld};
-  return gemm_dense(a_q, a_scales, a_fmt, a_scale_ld, w_q, w_scales, M, N, K, out, nullptr, 0,
-                    &qo, stream);
+  return gemm_dense(a_q, a_scales, a_fmt, a_scale_ld, w_q, w_scales, M, N, K, out, workspace,
+                    workspace_bytes, &qo, stream);
 }
 
 extern "C" bfq_status bfq_gemm_block_fp8_masked(

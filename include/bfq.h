@@ -224,8 +224,9 @@ bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, int32_t a_f
  *                  (packed UE8M0, a partial last word with zero bytes for its
  *                  missing groups); q_scale_ld >= M, q_scale_ld % 4 == 0;
  *                  columns M .. q_scale_ld-1 are not written.
- * K is never split (each thread quantizes whole 128-column output groups), so
- * no workspace is taken; small-m shapes run unsplit.
+ *   workspace      as for bfq_gemm_block_fp8 (same launch plan, same
+ *                  bfq_gemm_workspace_bytes); with K split, the cluster's
+ *                  reduction quantizes whole 128-column groups, one warp each.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE (also N % 128 != 0), MISALIGNED,
  * FORMAT, CUDA, DEVICE.
  */
@@ -233,7 +234,7 @@ bfq_status bfq_gemm_block_fp8_quant(const void* a_q, const void* a_scales, int32
                                     int64_t a_scale_ld, const void* w_q, const float* w_scales,
                                     int64_t M, int64_t N, int64_t K, void* out, int32_t q_fmt,
                                     void* q_out, void* q_scales, int64_t q_scale_ld,
-                                    void* stream);
+                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * bfq_gemm_block_fp8 for callers that cannot allocate device memory.  (The

@@ -30,12 +30,17 @@ def _problem(orc, bfq, M, N, K, a_fmt, seed):
     return (aq, sa, wq, sw), (d_aq, d_sa, d_wq, d_sw)
 
 
-def _fused(bfq, d, a_fmt, M, N, q_fmt, ld, with_out=True):
+def _fused(bfq, d, a_fmt, M, N, q_fmt, ld, with_out=True, split=True):
+    """split: pass the workspace the plain GEMM would use (K split over a
+    cluster where the plan splits); otherwise none (one CTA per tile)."""
+    K = d[0].shape[1]
     out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda") if with_out else None
     q = torch.full((M, N), 0x7E, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
     sc = torch.full((bfq.scale_cols(N, q_fmt), ld), SENT, dtype=torch.int32, device="cuda")
+    nbytes = bfq.bfq_gemm_workspace_bytes(M, N, K) if split else 0
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda") if nbytes else None
     bfq.bfq_gemm_block_fp8_quant(d[0], d[1], a_fmt, d[1].shape[-1], d[2], d[3], out, q_fmt, q, sc,
-                                 ld)
+                                 ld, workspace=ws)
     torch.cuda.synchronize()
     return out, q, sc
 
@@ -47,14 +52,15 @@ SHAPES = [(40, 384, 1024), (64, 128, 512), (130, 512, 640), (257, 1280, 384), (2
           (100, 16384, 256), (2048, 2560, 256)]
 
 
+@pytest.mark.parametrize("split", [True, False])
 @pytest.mark.parametrize("q_fmt", [0, 1, 2])
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_fused_output_quant_matches_quant_of_output(cuda_lib, orc, q_fmt, M, N, K):
+def test_fused_output_quant_matches_quant_of_output(cuda_lib, orc, q_fmt, M, N, K, split):
     bfq = cuda_lib
     a_fmt = 2 if q_fmt == 2 else 0
     (aq, sa, wq, sw), d = _problem(orc, bfq, M, N, K, a_fmt, seed=M + N + K + q_fmt)
     ld = bfq.align4(M) + 4
-    out, q, sc = _fused(bfq, d, a_fmt, M, N, q_fmt, ld)
+    out, q, sc = _fused(bfq, d, a_fmt, M, N, q_fmt, ld, split=split)
     # the bf16 output: within the GEMM tolerance of the oracle (sampled rows
     # for the large shape)
     rows = np.arange(M) if M <= 300 else np.unique(np.r_[0, M - 1, np.arange(5, M, 97)])
@@ -72,13 +78,14 @@ def test_fused_output_quant_matches_quant_of_output(cuda_lib, orc, q_fmt, M, N, 
 
 
 @pytest.mark.parametrize("q_fmt", [0, 2])
-@pytest.mark.parametrize("M,N,K", [(1152, 4096, 384), (2048, 2560, 256)])
+@pytest.mark.parametrize("M,N,K", [(24, 512, 4096), (130, 1280, 640), (1152, 4096, 384),
+                                   (2048, 2560, 256)])
 def test_fused_equals_unfused_chain_and_out_is_optional(cuda_lib, orc, q_fmt, M, N, K):
-    """Unsplit shapes: the fused codes, scales and bf16 output equal the
-    plain GEMM followed by the quant kernel; without the bf16 output the
-    codes and scales are unchanged."""
+    """Same launch plan as the plain GEMM (split along K for the first two,
+    one CTA per tile, persistent): the fused codes, scales and bf16 output
+    equal the plain GEMM followed by the quant kernel; without the bf16
+    output the codes and scales are unchanged."""
     bfq = cuda_lib
-    assert bfq.bfq_gemm_workspace_bytes(M, N, K) == 0
     a_fmt = 0
     _, d = _problem(orc, bfq, M, N, K, a_fmt, seed=7 + M + q_fmt)
     ld = bfq.align4(M)
@@ -106,10 +113,10 @@ def test_fused_quant_rejects_unsupported(cuda_lib):
     # N = 192 is not a multiple of 128: no whole output groups
     st = lib.bfq_gemm_block_fp8_quant(a.data_ptr(), s.data_ptr(), 0, 8, w.data_ptr(),
                                       sw.data_ptr(), 8, 192, 256, None, 0, q.data_ptr(),
-                                      qs.data_ptr(), 8, None)
+                                      qs.data_ptr(), 8, None, 0, None)
     assert bfq.STATUS_NAMES[st] == "BFQ_ERR_UNSUPPORTED_SHAPE"
     # scale leading dimension below M
     st = lib.bfq_gemm_block_fp8_quant(a.data_ptr(), s.data_ptr(), 0, 8, w.data_ptr(),
                                       sw.data_ptr(), 8, 128, 256, None, 0, q.data_ptr(),
-                                      qs.data_ptr(), 4, None)
+                                      qs.data_ptr(), 4, None, 0, None)
     assert bfq.STATUS_NAMES[st] == "BFQ_ERR_INVALID_ARG"
