@@ -442,9 +442,9 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
       // summing the partials in split order (deterministic).
       __threadfence();
       cluster_sync();
-      // The partials of the next unit are loaded before the current unit is
-      // summed and stored (its stores may alias the loads for the compiler),
-      // so each warp keeps a unit's loads in flight.
+      // Fused quant: the partials of a warp's next unit are loaded before the
+      // current unit is summed and stored (its byte stores may alias the loads
+      // for the compiler), so each warp keeps a unit's loads in flight.
       const float* ws = p.ws;
       const int64_t plane = (int64_t)p.M * p.N;
       auto load_parts = [&](int64_t off, float4 (&v)[kMaxSplits]) {
@@ -525,21 +525,14 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
         const int total = rows * upr;
         const int u_begin = (int)((int64_t)split * total / p.splits);
         const int u_end = (int)((int64_t)(split + 1) * total / p.splits);
-        auto unit_off = [&](int u) {
-          const int r = u / upr;
-          return (int64_t)(m0 + r) * p.N + n0 + (u - r * upr) * 4;
-        };
-        constexpr int kStep = C::kEpiWarps * 32;
-        float4 vn[kMaxSplits];
-        int u = u_begin + (int)threadIdx.x - C::kEpiWarp0 * 32;
-        if (u < u_end) load_parts(unit_off(u), vn);
-        for (; u < u_end; u += kStep) {
+        for (int u = u_begin + (int)threadIdx.x - C::kEpiWarp0 * 32; u < u_end;
+             u += C::kEpiWarps * 32) {
+          const int r = u / upr, c4 = u - (u / upr) * upr;
+          const int64_t off = (int64_t)(m0 + r) * p.N + n0 + c4 * 4;
           float4 v[kMaxSplits];
-#pragma unroll
-          for (int t = 0; t < kMaxSplits; ++t) v[t] = vn[t];
-          if (u + kStep < u_end) load_parts(unit_off(u + kStep), vn);
+          load_parts(off, v);
           const float4 a4 = sum_parts(v);
-          *reinterpret_cast<uint2*>(p.out + unit_off(u)) =
+          *reinterpret_cast<uint2*>(p.out + off) =
               make_uint2(pack_bf16x2(a4.x, a4.y), pack_bf16x2(a4.z, a4.w));
         }
       }
