@@ -73,6 +73,9 @@ def load_library(build: bool = True):
             "bfq_gemm_block_fp8_noalloc": (I32, [P, P, I32, I64, P, P, I64, I64, I64, P, P]),
             "bfq_gemm_block_fp8_quant": (I32, [P, P, I32, I64, P, P, I64, I64, I64, P, I32, P, P,
                                               I64, P, SZ, P]),
+            "bfq_interleave_gate_up": (I32, [P, P, I32, I64, I64, P, P, P]),
+            "bfq_gemm_block_fp8_masked_silu_quant": (I32, [P, P, I32, I64, P, P, P, I32, I32, I64,
+                                                          I64, I32, P, P, I64, P]),
             "bfq_gemm_noalloc_scratch_bytes": (SZ, []),
             "bfq_poll_device_status": (I32, [P]),
             "bfq_watchdog_selftest": (I32, [I32, P]),
@@ -189,6 +192,50 @@ def gemm_quant(a_q, a_scales, a_fmt: int, w_q, w_scales, q_fmt: int, out=None, s
     ws = gemm_workspace(M, N, a_q.shape[1], a_q.device)
     bfq_gemm_block_fp8_quant(a_q, a_scales, a_fmt, a_scales.shape[-1], w_q, w_scales, out, q_fmt,
                              q, sc, ld, workspace=ws, stream=stream)
+    return q, sc
+
+
+def bfq_interleave_gate_up(w_q, w_scales, w_q_out, w_scales_out, stream=None) -> None:
+    """[E, 2I, K] gate|up weight (and scales) -> 128-row blocks interleaved."""
+    lib = load_library()
+    E, N2, K = w_q.shape
+    _check("bfq_interleave_gate_up",
+           lib.bfq_interleave_gate_up(_ptr(w_q), _ptr(w_scales), E, N2 // 2, K, _ptr(w_q_out),
+                                      _ptr(w_scales_out), _stream(stream)))
+
+
+def interleave_gate_up(w_q, w_scales, stream=None):
+    """Allocating form of bfq_interleave_gate_up."""
+    w_o = torch.empty_like(w_q)
+    s_o = torch.empty_like(w_scales)
+    bfq_interleave_gate_up(w_q, w_scales, w_o, s_o, stream=stream)
+    return w_o, s_o
+
+
+def bfq_gemm_block_fp8_masked_silu_quant(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q,
+                                         w_scales, valid_counts, q_fmt: int, q_out, q_scales,
+                                         q_scale_ld: int, stream=None) -> None:
+    """Masked up projection (interleaved weights) with silu-mul-quant fused."""
+    lib = load_library()
+    E, T, K = a_q.shape
+    I = w_q.shape[1] // 2
+    _check("bfq_gemm_block_fp8_masked_silu_quant",
+           lib.bfq_gemm_block_fp8_masked_silu_quant(
+               _ptr(a_q), _ptr(a_scales), a_fmt, a_scale_ld, _ptr(w_q), _ptr(w_scales),
+               _ptr(valid_counts), E, T, I, K, q_fmt, _ptr(q_out), _ptr(q_scales), q_scale_ld,
+               _stream(stream)))
+
+
+def gemm_masked_silu_quant(a_q, a_scales, a_fmt: int, w_q, w_scales, valid_counts, q_fmt: int,
+                           stream=None):
+    """(q [E, T, I], scales [E, cols, T]) of silu(gate) * up of the masked up
+    projection; w_q / w_scales interleaved by interleave_gate_up."""
+    E, T, _ = a_q.shape
+    I = w_q.shape[1] // 2
+    q = torch.empty((E, T, I), dtype=torch.float8_e4m3fn, device=a_q.device)
+    sc = torch.empty((E, scale_cols(I, q_fmt), T), dtype=scale_dtype(q_fmt), device=a_q.device)
+    bfq_gemm_block_fp8_masked_silu_quant(a_q, a_scales, a_fmt, a_scales.shape[-1], w_q, w_scales,
+                                         valid_counts, q_fmt, q, sc, T, stream=stream)
     return q, sc
 
 

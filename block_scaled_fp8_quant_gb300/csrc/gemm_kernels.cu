@@ -608,7 +608,7 @@ __device__ __forceinline__ void persist_tile(int t, const GemmParams& p, const i
   }
 }
 
-template <bool MASKED, bool QOUT = false>
+template <bool MASKED, bool QOUT = false, bool SILU = false>
 __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
     gemm_block_fp8_persistent(const __grid_constant__ CUtensorMap tmA,
                               const __grid_constant__ CUtensorMap tmW,
@@ -616,6 +616,7 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
   constexpr int BN = 256;
   using C = GemmCfg<BN>;
   using PC = PersistCfg;
+  static_assert(!SILU || (MASKED && !QOUT), "the fused silu-mul-quant output is a masked form");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
@@ -824,7 +825,10 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
       const int m = m0 + row_local;
       const bool row_ok = m < m_limit;
       const int col0 = n0 + half * 128;
-      const bool warp_active = (m0 + quarter * 32 < m_limit) && (col0 < p.N);
+      // SILU: the tile's columns are gate block n0/256 (0..127) and the
+      // matching up block (128..255); warp half h accumulates gate and up
+      // columns h*64 .. h*64+63 of each, i.e. the same 64 features.
+      const bool warp_active = (m0 + quarter * 32 < m_limit) && (SILU || col0 < p.N);
       const int ncols = min(128, p.N - col0);
 
       uint64_t acc[64];
@@ -841,7 +845,8 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
           break;
         }
         const uint32_t a_bits = sc_a[slot * kBM + row_local];
-        const float w_s = __uint_as_float(sc_w[slot * 2 + half]);
+        const float w_s = __uint_as_float(sc_w[slot * 2 + (SILU ? 0 : half)]);
+        const float w_s_up = SILU ? __uint_as_float(sc_w[slot * 2 + 1]) : 0.0f;
         __syncwarp();
         if (lane == 0) mbar_arrive(&sempty[slot]);
         float sa_v;
@@ -852,35 +857,110 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
           sa_v = __uint_as_float(a_bits);
         }
         const uint64_t s2 = splat2(__fmul_rn(row_ok ? sa_v : 0.0f, w_s));
+        const uint64_t s2_up = SILU ? splat2(__fmul_rn(row_ok ? sa_v : 0.0f, w_s_up)) : 0ull;
         if (!mbar_wait(&tfull[buf], tph, abort_flag, p.status, kWaitTimeoutNs)) {
           stop = true;
           break;
         }
         tc_fence_after_sync();
         if (warp_active) {
-          const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                                 (uint32_t)(buf * BN + half * 128);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          if constexpr (SILU) {
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                   (uint32_t)(buf * BN + half * 64);
             uint64_t v[32];
-            tmem_ld64_pairs_wait(taddr + (uint32_t)(h * 64), v);
+            tmem_ld64_pairs_wait(taddr, v);  // gate columns
 #pragma unroll
-            for (int q = 0; q < 32; ++q) ffma2(acc[h * 32 + q], v[q], s2);
+            for (int q = 0; q < 32; ++q) ffma2(acc[q], v[q], s2);
+            tmem_ld64_pairs_wait(taddr + 128u, v);  // the matching up columns
+#pragma unroll
+            for (int q = 0; q < 32; ++q) ffma2(acc[32 + q], v[q], s2_up);
+          } else {
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                   (uint32_t)(buf * BN + half * 128);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint64_t v[32];
+              tmem_ld64_pairs_wait(taddr + (uint32_t)(h * 64), v);
+#pragma unroll
+              for (int q = 0; q < 32; ++q) ffma2(acc[h * 32 + q], v[q], s2);
+            }
           }
         }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
       }
-      // Every epilogue warp takes the same decision (the dense store below
-      // synchronises them on named barriers).
-      if (MASKED) {
+      // Every epilogue warp takes the same decision (the dense store and the
+      // fused silu-mul-quant below synchronise them on named barriers).
+      if (MASKED && !SILU) {
         if (stop || *abort_flag) break;
       } else if (named_barrier_or(2, C::kEpiWarps * 32, stop || *abort_flag)) {
         break;
       }
 
-      if (MASKED) {
+      if constexpr (SILU) {
+        // Fused silu(gate) * up + 1 x 128 group quant of the features of this
+        // tile, exactly as the silu-mul-quant kernel computes them from the
+        // bf16 up-projection output ("[EP+DP] Optimize the little operations
+        // in the DeepGEMM + DeepEP low latency case", Summary item 2): gate
+        // and up rounded to bf16, y = silu(g) * u in fp32, group amax over the
+        // 128 features (this thread's 64 and the other half-warp's 64,
+        // exchanged through shared memory), scale, codes.
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float2 gf = unpack2(acc[j]), uf = unpack2(acc[32 + j]);
+          const uint32_t gb = pack_bf16x2(gf.x, gf.y), ub = pack_bf16x2(uf.x, uf.y);
+          const float2 sg = bfq_silu2(bf16lo(gb), bf16hi(gb));
+          const float2 y = unpack2(mul2_rn(pack2(sg.x, sg.y), pack2(bf16lo(ub), bf16hi(ub))));
+          acc[j] = pack2(y.x, y.y);
+          amax = fmaxf(amax, fmaxf(fabsf(y.x), fabsf(y.y)));
+        }
+        float* xam = (float*)stg;  // [2][128] partial amax per half and row
+        xam[half * kBM + row_local] = amax;
+        named_barrier(1, C::kEpiWarps * 32);
+        amax = fmaxf(xam[row_local], xam[kBM + row_local]);
+        named_barrier(1, C::kEpiWarps * 32);  // both read before the next tile writes
+        if (warp_active && row_ok) {
+          const int I = p.N >> 1;
+          const int fg = n0 >> 8;  // 128-feature group of this tile
+          float sc = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
+          if (p.q_fmt != BFQ_SCALE_F32) sc = ceil_pow2(sc);
+          const float y_inv = __frcp_rn(sc);
+          uint8_t* qrow = p.q_out + ((int64_t)e * p.M + m) * I + fg * 128 + half * 64;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {  // 16 codes per 16-byte store
+            uint32_t w[4];
+#pragma unroll
+            for (int t2 = 0; t2 < 4; ++t2) {
+              const float2 y0 = unpack2(acc[c * 8 + 2 * t2]), y1 = unpack2(acc[c * 8 + 2 * t2 + 1]);
+              uint32_t lo, hi;
+              if (p.q_fmt == BFQ_SCALE_F32) {
+                lo = cvt_e4m3x2(group_div(y0.x, sc, y_inv), group_div(y0.y, sc, y_inv));
+                hi = cvt_e4m3x2(group_div(y1.x, sc, y_inv), group_div(y1.y, sc, y_inv));
+              } else {
+                lo = cvt_e4m3x2(__fmul_rn(y0.x, y_inv), __fmul_rn(y0.y, y_inv));
+                hi = cvt_e4m3x2(__fmul_rn(y1.x, y_inv), __fmul_rn(y1.y, y_inv));
+              }
+              w[t2] = lo | (hi << 16);
+            }
+            st_v4(qrow + c * 16, make_uint4(w[0], w[1], w[2], w[3]));
+          }
+          if (half == 0) {
+            const int G = I >> 7;
+            if (p.q_fmt == BFQ_SCALE_UE8M0_PACKED) {
+              const int64_t cols = (G + 3) >> 2;
+              uint8_t* word = (uint8_t*)p.q_scales +
+                              (((int64_t)e * cols + (fg >> 2)) * p.q_scale_ld + m) * 4;
+              word[fg & 3] = (uint8_t)ue8m0_byte(sc);
+              if (fg == G - 1)
+                for (int bb = (fg & 3) + 1; bb < 4; ++bb) word[bb] = 0;
+            } else {
+              ((float*)p.q_scales)[((int64_t)e * G + fg) * p.q_scale_ld + m] = sc;
+            }
+          }
+        }
+      } else if (MASKED) {
         if (warp_active && row_ok) {
           __nv_bfloat16* dst = p.out + (int64_t)e * p.out_estride + (int64_t)m * p.N + col0;
 #pragma unroll
@@ -1144,20 +1224,20 @@ Plan masked_plan(const DeviceInfo& dev, int64_t E, int64_t T, int64_t N, int64_t
   return pl;
 }
 
-template <bool MASKED, bool QOUT = false>
+template <bool MASKED, bool QOUT = false, bool SILU = false>
 bfq_status configure_persistent(const DeviceInfo& dev) {
   static bool configured[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (configured[dev.ordinal]) return BFQ_OK;
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, gemm_block_fp8_persistent<MASKED, QOUT>) != cudaSuccess) {
+  if (cudaFuncGetAttributes(&fa, gemm_block_fp8_persistent<MASKED, QOUT, SILU>) != cudaSuccess) {
     cudaGetLastError();
     return BFQ_ERR_CUDA;
   }
   // setmaxnreg.inc only completes if the launch allocation covers the split
   if (fa.numRegs != GemmCfg<256>::kLaunchRegs) return BFQ_ERR_DEVICE;
-  if (cudaFuncSetAttribute(gemm_block_fp8_persistent<MASKED, QOUT>,
+  if (cudaFuncSetAttribute(gemm_block_fp8_persistent<MASKED, QOUT, SILU>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)PersistCfg::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
@@ -1167,13 +1247,13 @@ bfq_status configure_persistent(const DeviceInfo& dev) {
   return BFQ_OK;
 }
 
-template <bool MASKED, bool QOUT = false>
+template <bool MASKED, bool QOUT = false, bool SILU = false>
 bfq_status launch_persistent(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
                              const CUtensorMap& mo, const GemmParams& p, unsigned grid,
                              cudaStream_t s) {
-  bfq_status st = configure_persistent<MASKED, QOUT>(dev);
+  bfq_status st = configure_persistent<MASKED, QOUT, SILU>(dev);
   if (st != BFQ_OK) return st;
-  return launch_status(launch_pdl(gemm_block_fp8_persistent<MASKED, QOUT>, dim3(grid),
+  return launch_status(launch_pdl(gemm_block_fp8_persistent<MASKED, QOUT, SILU>, dim3(grid),
                                   dim3(GemmCfg<256>::kThreads), PersistCfg::kSmemBytes, s, 1u, ma,
                                   mw, mo, p));
 }
@@ -1419,4 +1499,109 @@ extern "C" bfq_status bfq_gemm_block_fp8_noalloc(const void* a_q, const void* a_
   }
   return bfq_gemm_block_fp8(a_q, a_scales, a_fmt, a_scale_ld, w_q, w_scales, M, N, K, out,
                             scratch, need > 0 ? bfq::kNoAllocScratchBytes : 0, stream);
+}
+
+// ----------------------------------------------------------------------------
+// masked up projection with silu-mul-quant fused into its epilogue
+// ----------------------------------------------------------------------------
+namespace bfq {
+namespace {
+
+// Copies 128-row blocks of each expert's [2I][K] weight (and the matching
+// scale rows) so that output block 2j is gate block j and block 2j+1 is up
+// block j.  One CTA per (output block, expert); 16-byte copies.
+__global__ void __launch_bounds__(256)
+    interleave_gate_up_kernel(const uint8_t* __restrict__ w, const float* __restrict__ sw,
+                              int64_t I, int64_t K, uint8_t* __restrict__ w_out,
+                              float* __restrict__ sw_out) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int64_t nb = blockIdx.x, e = blockIdx.y;
+  const int64_t G = I / 128, KB = K / 128;
+  const int64_t src_blk = (nb & 1) ? G + (nb >> 1) : (nb >> 1);
+  const uint4* src = (const uint4*)(w + (e * 2 * I + src_blk * 128) * K);
+  uint4* dst = (uint4*)(w_out + (e * 2 * I + nb * 128) * K);
+  const int64_t n16 = 128 * K / 16;
+  for (int64_t i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src[i];
+  const float* ssrc = sw + (e * 2 * G + src_blk) * KB;
+  float* sdst = sw_out + (e * 2 * G + nb) * KB;
+  for (int64_t i = threadIdx.x; i < KB; i += blockDim.x) sdst[i] = ssrc[i];
+}
+
+}  // namespace
+}  // namespace bfq
+
+extern "C" bfq_status bfq_interleave_gate_up(const void* w_q, const float* w_scales, int32_t E,
+                                             int64_t I, int64_t K, void* w_q_out,
+                                             float* w_scales_out, void* stream) {
+  if (E <= 0 || I <= 0 || K <= 0) return BFQ_ERR_INVALID_ARG;
+  if (I % 128 != 0 || K % 128 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (E > 65535 || 2 * I / 128 > 0x7FFFFFFF) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (!w_q || !w_scales || !w_q_out || !w_scales_out) return BFQ_ERR_INVALID_ARG;
+  if (w_q == w_q_out || w_scales == w_scales_out) return BFQ_ERR_INVALID_ARG;
+  if (!aligned16(w_q) || !aligned16(w_q_out) || ((uintptr_t)w_scales & 3u) ||
+      ((uintptr_t)w_scales_out & 3u))
+    return BFQ_ERR_MISALIGNED;
+  DeviceInfo dev;
+  bfq_status st = current_device(&dev);
+  if (st != BFQ_OK) return st;
+  return launch_status(launch_pdl(interleave_gate_up_kernel, dim3((unsigned)(2 * I / 128),
+                                                                   (unsigned)E),
+                                  dim3(256), 0, (cudaStream_t)stream, 1u,
+                                  (const uint8_t*)w_q, w_scales, I, K, (uint8_t*)w_q_out,
+                                  w_scales_out));
+}
+
+extern "C" bfq_status bfq_gemm_block_fp8_masked_silu_quant(
+    const void* a_q, const void* a_scales, int32_t a_fmt, int64_t a_scale_ld, const void* w_q,
+    const float* w_scales, const int32_t* valid_counts, int32_t E, int32_t T, int64_t I,
+    int64_t K, int32_t q_fmt, void* q_out, void* q_scales, int64_t q_scale_ld, void* stream) {
+  if (E < 0 || T < 0 || I <= 0 || K <= 0 || !valid_fmt(a_fmt) || !valid_fmt(q_fmt) ||
+      a_scale_ld < T || q_scale_ld < T)
+    return BFQ_ERR_INVALID_ARG;
+  if (K % 128 != 0 || I % 128 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  const int64_t N = 2 * I;
+  if ((int64_t)E * T > 0x7FFFFFFF || (int64_t)E * N > 0x7FFFFFFF || K > 0x7FFFFFFF ||
+      (int64_t)T * I > 0x7FFFFFFF)
+    return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (E > kPersistMaxExperts) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (E == 0 || T == 0) return BFQ_OK;
+  if (!a_q || !a_scales || !w_q || !w_scales || !valid_counts || !q_out || !q_scales)
+    return BFQ_ERR_INVALID_ARG;
+  if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(q_out) || a_scale_ld % 4 != 0 ||
+      q_scale_ld % 4 != 0 || ((uintptr_t)a_scales & 3u) || ((uintptr_t)w_scales & 3u) ||
+      ((uintptr_t)q_scales & 3u))
+    return BFQ_ERR_MISALIGNED;
+  DeviceInfo dev;
+  bfq_status st = check_device(&dev);
+  if (st != BFQ_OK) return st;
+  if (dev.smem_optin < PersistCfg::kSmemBytes) return BFQ_ERR_DEVICE;
+  CUtensorMap ma, mw;
+  if (!make_map(&ma, a_q, (uint64_t)K, (uint64_t)E * T, kBM) ||
+      !make_map(&mw, w_q, (uint64_t)K, (uint64_t)E * N, 256u))
+    return BFQ_ERR_CUDA;
+  GemmParams p{};
+  p.sa = a_scales;
+  p.sa_ld = a_scale_ld;
+  p.sa_estride = scale_cols(K, a_fmt) * a_scale_ld;
+  p.sw = w_scales;
+  p.sw_estride = (N / 128) * (K / 128);
+  p.counts = valid_counts;
+  p.status = device_status_ptr();
+  if (!p.status) return BFQ_ERR_CUDA;
+  p.M = T;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.m_tiles = (int)cdiv(T, kBM);
+  p.n_tiles = (int)(N / 256);
+  p.splits = 1;
+  p.a_fmt = a_fmt;
+  p.E = E;
+  p.q_out = (uint8_t*)q_out;
+  p.q_scales = q_scales;
+  p.q_scale_ld = q_scale_ld;
+  p.q_fmt = q_fmt;
+  const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles * E;
+  const unsigned grid = (unsigned)(tiles < dev.sm_count ? tiles : dev.sm_count);
+  return launch_persistent<true, false, true>(dev, ma, mw, mw, p, grid, (cudaStream_t)stream);
 }

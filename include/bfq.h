@@ -297,6 +297,57 @@ bfq_status bfq_gemm_block_fp8_masked(const void* a_q, const void* a_scales, int3
                                      size_t workspace_bytes, void* stream);
 
 /*
+ * Reorders an MoE up-projection weight for the fused form below: each
+ * expert's [2I][K] e4m3 weight (gate rows 0..I-1, up rows I..2I-1, the
+ * split of "[EP+DP] Optimize the little operations in the DeepGEMM + DeepEP
+ * low latency case" silu-and-mul) and its [2I/128][K/128] block scales are
+ * copied so that 128-row block 2j is gate block j and block 2j+1 is up
+ * block j.  A one-time layout step (as weight quant is), on the GPU.
+ *
+ *   w_q, w_scales           e4m3 [E][2I][K] (16-byte aligned), float
+ *                           [E][2I/128][K/128]
+ *   w_q_out, w_scales_out   same shapes, distinct buffers
+ *   I % 128 == 0, K % 128 == 0.
+ * Errors: INVALID_ARG (also in-place), UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+bfq_status bfq_interleave_gate_up(const void* w_q, const float* w_scales, int32_t E, int64_t I,
+                                  int64_t K, void* w_q_out, float* w_scales_out, void* stream);
+
+/*
+ * Masked grouped up-projection GEMM with silu-and-mul and its quant fused
+ * into the epilogue: for expert e and row r < valid_counts[e],
+ *
+ *   h[e, r, :]  = bf16(GEMM of bfq_gemm_block_fp8_masked with the
+ *                 un-interleaved weight), 2I columns (gate | up)
+ *   q_out, q_scales = bfq_silu_mul_quant(h, valid_counts, q_fmt)
+ *
+ * bit for bit, without writing h: each 256-wide tile holds a gate block and
+ * its up block (weights from bfq_interleave_gate_up), so the epilogue forms
+ * y = silu(gate) * up for 128 features of a row and quantizes them as one
+ * 1 x 128 group.  Rows r >= count are neither computed nor written (only row
+ * tiles below the count are scheduled, as in bfq_gemm_block_fp8_masked).
+ *
+ *   a_q .. a_scale_ld   as for bfq_gemm_block_fp8_masked (K of the up
+ *                       projection, E <= 1024).
+ *   w_q, w_scales       interleaved (bfq_interleave_gate_up).
+ *   I                   features per expert (the down projection's K),
+ *                       I % 128 == 0.
+ *   q_fmt, q_out, q_scales, q_scale_ld   the output of bfq_silu_mul_quant:
+ *                       e4m3 [E][T][I]; scales [E][cols][q_scale_ld] with
+ *                       cols = I/128 (fp32, pow2) or ceil(I/512) (packed
+ *                       UE8M0); q_scale_ld >= T, % 4 == 0.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE (also E > 1024), MISALIGNED, CUDA,
+ * DEVICE.
+ */
+bfq_status bfq_gemm_block_fp8_masked_silu_quant(const void* a_q, const void* a_scales,
+                                                int32_t a_fmt, int64_t a_scale_ld,
+                                                const void* w_q, const float* w_scales,
+                                                const int32_t* valid_counts, int32_t E,
+                                                int32_t T, int64_t I, int64_t K, int32_t q_fmt,
+                                                void* q_out, void* q_scales, int64_t q_scale_ld,
+                                                void* stream);
+
+/*
  * Reads and clears the device-side error latch that kernel watchdogs set when
  * a bounded wait (on a TMA/MMA barrier) gives up.  Synchronizes `stream`.
  * Returns BFQ_OK, BFQ_ERR_TIMEOUT, or BFQ_ERR_CUDA.
