@@ -569,6 +569,28 @@ def measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, reps):
                              "gbps_b2b": round(gbs_b2b, 1),
                              "hbm_frac_b2b": round(gbs_b2b / hbm_peak, 3), "bytes": nbytes}
     del hs
+    # the slice with the up projection's silu-and-mul + quant fused into its
+    # epilogue (weights interleaved once, as offline weight preparation)
+    w_up_i, s_up_i = bfq.interleave_gate_up(w_up, s_up)
+
+    def up_act_fused():
+        bfq.bfq_gemm_block_fp8_masked_silu_quant(a_up, sa_up, 2, T, w_up_i, s_up_i, d_counts, 2,
+                                                 a_dn, sa_dn, T)
+
+    up_act_fused()
+    torch.cuda.synchronize()
+    us_fused = gated_times(torch, up_act_fused, reps)
+    us_seq = {}
+    for name, fns in (("unfused", (up, act, down)), ("fused", (up_act_fused, down))):
+        def chain(i, fns=fns):
+            for fn in fns:
+                fn()
+        us_seq[name] = graph_back_to_back_us(torch, chain, 1, 6)
+    res["up_silu_quant_fused"] = {"us": round(us_fused, 2),
+                                  "unfused_up_plus_silu_us": round(res["up_gemm"]["us"] +
+                                                                   res["silu_mul_quant"]["us"], 2)}
+    res["slice_us_b2b"] = {k: round(v, 2) for k, v in us_seq.items()}
+    del w_up_i, s_up_i
     del w_up, w_dn, x, h
     return res
 

@@ -907,14 +907,16 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
         // 128 features (this thread's 64 and the other half-warp's 64,
         // exchanged through shared memory), scale, codes.
         float amax = 0.0f;
+        if (warp_active && row_ok) {  // rows past the count: nothing to form
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float2 gf = unpack2(acc[j]), uf = unpack2(acc[32 + j]);
-          const uint32_t gb = pack_bf16x2(gf.x, gf.y), ub = pack_bf16x2(uf.x, uf.y);
-          const float2 sg = bfq_silu2(bf16lo(gb), bf16hi(gb));
-          const float2 y = unpack2(mul2_rn(pack2(sg.x, sg.y), pack2(bf16lo(ub), bf16hi(ub))));
-          acc[j] = pack2(y.x, y.y);
-          amax = fmaxf(amax, fmaxf(fabsf(y.x), fabsf(y.y)));
+          for (int j = 0; j < 32; ++j) {
+            const float2 gf = unpack2(acc[j]), uf = unpack2(acc[32 + j]);
+            const uint32_t gb = pack_bf16x2(gf.x, gf.y), ub = pack_bf16x2(uf.x, uf.y);
+            const float2 sg = bfq_silu2(bf16lo(gb), bf16hi(gb));
+            const float2 y = unpack2(mul2_rn(pack2(sg.x, sg.y), pack2(bf16lo(ub), bf16hi(ub))));
+            acc[j] = pack2(y.x, y.y);
+            amax = fmaxf(amax, fmaxf(fabsf(y.x), fabsf(y.y)));
+          }
         }
         float* xam = (float*)stg;  // [2][128] partial amax per half and row
         xam[half * kBM + row_local] = amax;
