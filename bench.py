@@ -184,6 +184,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 SAMPLE_ROWS = 8
 SAMPLE_COLS = 1024
+CPU_BASELINE_SECONDS = 10.0
 
 
 def oracle_sample_step():
@@ -212,13 +213,17 @@ def cpu_baseline():
     import oracle
 
     oracle.build_oracle()
+    # Repeat the bounded sample until about 10 s of CPU work has been timed.
     t0 = time.perf_counter()
-    flops = oracle_sample_step()
+    flops, reps = 0, 0
+    while reps == 0 or time.perf_counter() - t0 < CPU_BASELINE_SECONDS:
+        flops += oracle_sample_step()
+        reps += 1
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{SAMPLE_ROWS} activation rows x first {SAMPLE_COLS} weight rows of "
-                      f"each of the 6 (n,k) sweep shapes: weight block quant + activation "
-                      f"quant + fp64 block GEMM, single thread ({dt:.1f} s)"}
+            "sample": f"{reps} x ({SAMPLE_ROWS} activation rows x first {SAMPLE_COLS} weight "
+                      f"rows of each of the 6 (n,k) sweep shapes: weight block quant + "
+                      f"activation quant + fp64 block GEMM), single thread ({dt:.1f} s)"}
 
 
 def run_reference(args, rank, world):
