@@ -242,7 +242,7 @@ def gemm_masked_silu_quant(a_q, a_scales, a_fmt: int, w_q, w_scales, valid_count
 def bfq_gemm_block_fp8_noalloc(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w_scales, out,
                                stream=None) -> None:
     """bfq_gemm_block_fp8 without a workspace argument: for callers that may not
-    allocate device memory (see include/bfq.h).  Calls must not overlap on the GPU."""
+    allocate device memory (see include/bfq.h)."""
     lib = load_library()
     M, K = a_q.shape
     N = w_q.shape[0]
@@ -314,7 +314,8 @@ _ws_cache: dict = {}
 
 
 def gemm_workspace(M: int, N: int, K: int, device) -> torch.Tensor | None:
-    """Zero-initialised workspace sized for (M, N, K) on `device` (cached, grows)."""
+    """Zero-initialised workspace sized for (M, N, K) on `device` (cached, grows);
+    None when the plan needs none (every plan of the current kernels)."""
     need = bfq_gemm_workspace_bytes(M, N, K)
     if need == 0:
         return None

@@ -73,7 +73,6 @@ struct GemmParams {
   int64_t sw_estride;      // floats of sw per expert (masked)
   __nv_bfloat16* out;      // [rows][N]
   int64_t out_estride;     // elements of out per expert (masked)
-  float* ws;               // split-K partials [splits][M][N]
   const int32_t* counts;   // masked: per-expert valid rows
   int* status;             // device error latch
   int M;                   // dense: rows of A; masked: rows per expert (T)
@@ -317,7 +316,10 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
       asm volatile("cp.async.wait_all;" ::: "memory");
     }
     __syncwarp();
-    if (p.splits > 1) cluster_sync();  // pairs with the epilogue's barrier
+    if (p.splits > 1) {  // pair with the epilogue's two cluster barriers
+      cluster_sync();
+      cluster_sync();
+    }
   } else {
     if (C::kRegSplit) setmaxnreg_inc<C::kEpilogueRegs>();
     // ------------------------- epilogue / promotion ---------------------------
@@ -427,30 +429,38 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
       }
     } else {
       // split-K: publish this split's fp32 partial; the cluster reduces below.
+      // split-K: this split's fp32 partial stays in the CTA's own shared
+      // memory, in the (now idle) stage ring: every load has landed and every
+      // MMA that read a stage has completed.  Row r of the tile holds BN
+      // floats; 16-byte chunk j sits at chunk j ^ (r mod 8) (conflict-free
+      // both for the row-per-thread writes here and the chunk-per-thread
+      // reads below).  The K splits of one tile are one thread-block cluster:
+      // after one cluster barrier, CTA `split` sums the split-th slice of the
+      // tile over the splits' partials, read from the peers' shared memory in
+      // split order (deterministic); a second barrier keeps every partial in
+      // place until all peers have read it.
+      static_assert(kBM * BN * 4 <= C::kStages * C::kStageBytes, "partial exceeds the stages");
+      const uint32_t part_base = smem_u32(smem);
+      auto part_addr = [&](int r, int j) {
+        return part_base + (uint32_t)(r * BN * 4) + (uint32_t)((j ^ (r & 7)) << 4);
+      };
       if (ok && warp_active && row_ok) {
-        float* part = p.ws + ((int64_t)split * p.M + m) * p.N + col0;
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          if (c * 4 < ncols) {
-            const float2 f0 = unpack2(acc[c * 2]), f1 = unpack2(acc[c * 2 + 1]);
-            *reinterpret_cast<float4*>(part + c * 4) = make_float4(f0.x, f0.y, f1.x, f1.y);
-          }
+          if (c * 4 < ncols)
+            st_shared_v4(part_addr(row_local, half * 32 + c),
+                         make_uint4((uint32_t)acc[c * 2], (uint32_t)(acc[c * 2] >> 32),
+                                    (uint32_t)acc[c * 2 + 1], (uint32_t)(acc[c * 2 + 1] >> 32)));
       }
-      // The K splits of one tile are one thread-block cluster.  After every
-      // CTA has published its partial (every thread of the cluster passes one
-      // cluster barrier), CTA `split` reduces the split-th slice of the tile,
-      // summing the partials in split order (deterministic).
-      __threadfence();
       cluster_sync();
       // Fused quant: the partials of a warp's next unit are loaded before the
       // current unit is summed and stored (its byte stores may alias the loads
       // for the compiler), so each warp keeps a unit's loads in flight.
-      const float* ws = p.ws;
-      const int64_t plane = (int64_t)p.M * p.N;
-      auto load_parts = [&](int64_t off, float4 (&v)[kMaxSplits]) {
+      auto load_parts = [&](int r, int j, float4 (&v)[kMaxSplits]) {
+        const uint32_t a = part_addr(r, j);
 #pragma unroll
         for (int t = 0; t < kMaxSplits; ++t)
-          if (t < p.splits) v[t] = __ldcg(reinterpret_cast<const float4*>(ws + t * plane + off));
+          if (t < p.splits) v[t] = ld_dsmem_v4(dsmem_addr(a, (uint32_t)t));
       };
       auto sum_parts = [&](const float4 (&v)[kMaxSplits]) {  // in split order
         float4 a4 = v[0];
@@ -471,18 +481,18 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
         const int total = rows * gpr;
         const int u_begin = (int)((int64_t)split * total / p.splits);
         const int u_end = (int)((int64_t)(split + 1) * total / p.splits);
-        auto unit_off = [&](int u) {
+        auto load_unit = [&](int u, float4 (&v)[kMaxSplits]) {
           const int r = u / gpr;
-          return (int64_t)(m0 + r) * p.N + n0 + (u - r * gpr) * 128 + lane * 4;
+          load_parts(r, (u - r * gpr) * 32 + lane, v);
         };
         float4 vn[kMaxSplits];
         int u = u_begin + (warp - C::kEpiWarp0);
-        if (u < u_end) load_parts(unit_off(u), vn);
+        if (u < u_end) load_unit(u, vn);
         for (; u < u_end; u += C::kEpiWarps) {
           float4 v[kMaxSplits];
 #pragma unroll
           for (int t = 0; t < kMaxSplits; ++t) v[t] = vn[t];
-          if (u + C::kEpiWarps < u_end) load_parts(unit_off(u + C::kEpiWarps), vn);
+          if (u + C::kEpiWarps < u_end) load_unit(u + C::kEpiWarps, vn);
           const int r = u / gpr;
           const int col = n0 + (u - r * gpr) * 128;
           const int64_t off = (int64_t)(m0 + r) * p.N + col + lane * 4;
@@ -530,12 +540,13 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
           const int r = u / upr, c4 = u - (u / upr) * upr;
           const int64_t off = (int64_t)(m0 + r) * p.N + n0 + c4 * 4;
           float4 v[kMaxSplits];
-          load_parts(off, v);
+          load_parts(r, c4, v);
           const float4 a4 = sum_parts(v);
           *reinterpret_cast<uint2*>(p.out + off) =
               make_uint2(pack_bf16x2(a4.x, a4.y), pack_bf16x2(a4.z, a4.w));
         }
       }
+      cluster_sync();  // the peers have read this CTA's partial
     }
   }
 
@@ -1080,24 +1091,14 @@ struct Plan {
   int bn = 256;
   bool persist = false;  // persistent 256-wide kernel (no K split)
   int m_tiles = 0, n_tiles = 0, splits = 1;
-  size_t ws_bytes = 0;  // bytes needed by this plan
 };
-
-// Workspace of a split-K plan: the fp32 partial sums [splits][M][N].  Every
-// element a call reads was written earlier in the same call, so the buffer
-// needs no initialisation and one buffer serves calls of any shape.
-size_t split_ws_bytes(int64_t M, int64_t N, int splits) {
-  if (splits <= 1) return 0;
-  return (size_t)splits * (size_t)M * (size_t)N * sizeof(float);
-}
 
 template <int BN>
 int max_active_clusters(const DeviceInfo& dev, int cluster);
 
 // Plan for one tile width: K is split over a cluster of CTAs when there are
 // fewer tiles than SMs.
-Plan plan_for_width(const DeviceInfo& dev, int bn, int64_t M, int64_t N, int64_t K,
-                    size_t ws_avail, bool limit_by_ws) {
+Plan plan_for_width(const DeviceInfo& dev, int bn, int64_t M, int64_t N, int64_t K) {
   Plan pl;
   pl.bn = bn;
   pl.m_tiles = (int)cdiv(M, kBM);
@@ -1113,27 +1114,22 @@ Plan plan_for_width(const DeviceInfo& dev, int bn, int64_t M, int64_t N, int64_t
   while (splits > 1 && (pl.bn == 256 ? max_active_clusters<256>(dev, splits)
                                      : max_active_clusters<128>(dev, splits)) < tiles)
     --splits;
-  if (limit_by_ws)
-    while (splits > 1 && split_ws_bytes(M, N, splits) > ws_avail) --splits;
   pl.splits = splits;
-  pl.ws_bytes = split_ws_bytes(M, N, splits);
   return pl;
 }
 
-// 256-wide tiles, except where 128-wide tiles need no K split at all and
-// keep at least as many CTAs busy: that drops the fp32 partial sums a split
-// tile writes and its cluster reads back (splits x M x N x 4 bytes each way)
-// and lets the tile leave through the TMA-store epilogue.  This pays once the
-// tile holds more than 32 rows; with fewer rows the partials are small and
-// the 256-wide tile's larger weight stages (more bytes in flight per SM) win.
-Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, size_t ws_avail,
-                bool limit_by_ws) {
-  Plan pl = plan_for_width(dev, N > 128 ? 256 : 128, M, N, K, ws_avail, limit_by_ws);
+// 256-wide tiles, except where the 256-wide plan splits K and 128-wide tiles
+// keep more CTAs busy, or as many with no K split at all (no partial sums to
+// reduce, and the tile leaves through the TMA-store epilogue).  This pays
+// once the tile holds more than 32 rows; with fewer rows the 256-wide tile's
+// larger weight stages (more bytes in flight per SM) win.
+Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K) {
+  Plan pl = plan_for_width(dev, N > 128 ? 256 : 128, M, N, K);
   if (pl.bn == 256 && pl.splits > 1 && M > 32) {
-    const Plan alt = plan_for_width(dev, 128, M, N, K, ws_avail, limit_by_ws);
-    if (alt.splits == 1 &&
-        alt.m_tiles * alt.n_tiles >= pl.m_tiles * pl.n_tiles * pl.splits)
-      pl = alt;
+    const Plan alt = plan_for_width(dev, 128, M, N, K);
+    const int ctas = pl.m_tiles * pl.n_tiles * pl.splits;
+    const int alt_ctas = alt.m_tiles * alt.n_tiles * alt.splits;
+    if (alt_ctas > ctas || (alt.splits == 1 && alt_ctas >= ctas)) pl = alt;
   }
   // More 256-wide tiles than SMs: one persistent CTA per SM walks them.
   if (pl.bn == 256 && pl.splits == 1 && pl.m_tiles * pl.n_tiles > dev.sm_count &&
@@ -1273,11 +1269,13 @@ bfq_status check_device(DeviceInfo* dev) {
 
 using namespace bfq;
 
+// The K splits of a tile reduce through distributed shared memory, so no
+// plan needs a workspace.
 extern "C" size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  if (M <= 0 || N <= 0 || K <= 0 || K % 128 != 0) return 0;
-  DeviceInfo dev;
-  if (current_device(&dev) != BFQ_OK) return 0;
-  return dense_plan(dev, M, N, K, 0, false).ws_bytes;
+  (void)M;
+  (void)N;
+  (void)K;
+  return 0;
 }
 
 namespace bfq {
@@ -1316,7 +1314,7 @@ bfq_status gemm_dense(const void* a_q, const void* a_scales, int32_t a_fmt, int6
   DeviceInfo dev;
   bfq_status st = check_device(&dev);
   if (st != BFQ_OK) return st;
-  Plan pl = dense_plan(dev, M, N, K, workspace ? workspace_bytes : 0, true);
+  Plan pl = dense_plan(dev, M, N, K);
   CUtensorMap ma, mw, mo;
   if (!make_map(&ma, a_q, (uint64_t)K, (uint64_t)M, kBM) ||
       !make_map(&mw, w_q, (uint64_t)K, (uint64_t)N, (uint32_t)pl.bn))
@@ -1343,7 +1341,6 @@ bfq_status gemm_dense(const void* a_q, const void* a_scales, int32_t a_fmt, int6
     p.q_scale_ld = qo->scale_ld;
     p.q_fmt = qo->fmt;
   }
-  if (pl.splits > 1) p.ws = (float*)workspace;
   const unsigned grid = (unsigned)(pl.m_tiles * pl.n_tiles * pl.splits);
   const unsigned pgrid = grid < (unsigned)dev.sm_count ? grid : (unsigned)dev.sm_count;
   cudaStream_t s = (cudaStream_t)stream;
@@ -1445,62 +1442,18 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked(
 // captured in global mode (allocation is an error there), plugins inside a
 // host framework that owns every byte of device memory, and serving loops
 // that forbid allocation after start-up because cudaMalloc can synchronize
-// the device.  For them the split-K scratch lives in this file-scope device
-// array, which every GPU that loads the library holds until the process
-// exits.  In host code the array's name is only a host-side stand-in; its
-// device address is looked up with cudaGetSymbolAddress, once per device,
-// with that device current.
+// the device.  The K splits reduce through distributed shared memory, so no
+// plan needs scratch: this is the regular call without a workspace.
 // ----------------------------------------------------------------------------
-namespace bfq {
-namespace {
-
-constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;  // 32 MiB
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-
-void* g_noalloc_ptr[64];
-std::mutex g_noalloc_mu;
-
-// Device address of the scratch array on the current device (set-up on the
-// first call per device).  Returns BFQ_OK or BFQ_ERR_CUDA.
-bfq_status noalloc_scratch(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    cudaGetLastError();
-    return BFQ_ERR_CUDA;
-  }
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return BFQ_ERR_CUDA;
-    }
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
-  return BFQ_OK;
-}
-
-}  // namespace
-}  // namespace bfq
-
-extern "C" size_t bfq_gemm_noalloc_scratch_bytes(void) { return bfq::kNoAllocScratchBytes; }
+extern "C" size_t bfq_gemm_noalloc_scratch_bytes(void) { return 0; }
 
 extern "C" bfq_status bfq_gemm_block_fp8_noalloc(const void* a_q, const void* a_scales,
                                                  int32_t a_fmt, int64_t a_scale_ld,
                                                  const void* w_q, const float* w_scales,
                                                  int64_t M, int64_t N, int64_t K, void* out,
                                                  void* stream) {
-  // The plan's scratch must fit the static array; larger plans are refused.
-  const size_t need = bfq_gemm_workspace_bytes(M, N, K);
-  if (need > bfq::kNoAllocScratchBytes) return BFQ_ERR_WORKSPACE;
-  void* scratch = nullptr;
-  if (need > 0) {
-    bfq_status st = bfq::noalloc_scratch(&scratch);
-    if (st != BFQ_OK) return st;
-  }
   return bfq_gemm_block_fp8(a_q, a_scales, a_fmt, a_scale_ld, w_q, w_scales, M, N, K, out,
-                            scratch, need > 0 ? bfq::kNoAllocScratchBytes : 0, stream);
+                            nullptr, 0, stream);
 }
 
 // ----------------------------------------------------------------------------

@@ -160,11 +160,11 @@ bfq_status bfq_weight_block_quant(const void* w, int64_t batch, int64_t N, int64
                                   int32_t fmt, void* wq, float* sw, void* stream);
 
 /*
- * Bytes of workspace that bfq_gemm_block_fp8 can use for an (M, N, K) problem
- * on the current device: 0 when the launch plan does not split K, else the
- * fp32 partial sums of the K splits, [splits][M][N].  The buffer needs no
- * initialisation (each call writes every element it reads) and serves calls
- * of any shape; calls that share one must not overlap in time.
+ * Bytes of workspace that bfq_gemm_block_fp8 needs for an (M, N, K) problem:
+ * 0 for every problem.  The K splits of a tile reduce their fp32 partial sums
+ * through the distributed shared memory of their thread-block cluster, so no
+ * plan uses global scratch.  Kept so that callers written against a
+ * workspace-taking interface need not change.
  */
 size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
@@ -177,8 +177,9 @@ size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *
  * with fp32 accumulation on the tensor cores and the scale product applied
  * to each 128-deep K block ("promotion").  When there are fewer output tiles
- * than SMs, K is split over the CTAs of a thread-block cluster (at most 8)
- * and the partial sums are added in split order, so results are
+ * than SMs, K is split over the CTAs of a thread-block cluster (at most 8);
+ * each CTA keeps its fp32 partial sum in shared memory and the cluster adds
+ * them in split order through distributed shared memory, so results are
  * deterministic.
  *
  *   a_q            e4m3 [M][K], 16-byte aligned.
@@ -190,9 +191,9 @@ size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   M, N, K        M >= 0 (0 = no-op), N > 0, N % 64 == 0, K > 0,
  *                  K % 128 == 0.
  *   out            bf16 [M][N] (preallocated by the caller).
- *   workspace      device buffer of workspace_bytes (may be NULL / 0); when
- *                  smaller than bfq_gemm_workspace_bytes() the call uses a
- *                  plan that fits (fewer K splits), never an error.
+ *   workspace      unused by the current plans (may be NULL / 0); a non-NULL
+ *                  workspace must be 16-byte aligned, and workspace_bytes > 0
+ *                  with a NULL workspace is INVALID_ARG.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, FORMAT, CUDA, DEVICE.
  */
 bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, int32_t a_fmt,
@@ -224,9 +225,9 @@ bfq_status bfq_gemm_block_fp8(const void* a_q, const void* a_scales, int32_t a_f
  *                  (packed UE8M0, a partial last word with zero bytes for its
  *                  missing groups); q_scale_ld >= M, q_scale_ld % 4 == 0;
  *                  columns M .. q_scale_ld-1 are not written.
- *   workspace      as for bfq_gemm_block_fp8 (same launch plan, same
- *                  bfq_gemm_workspace_bytes); with K split, the cluster's
- *                  reduction quantizes whole 128-column groups, one warp each.
+ *   workspace      as for bfq_gemm_block_fp8 (unused; same launch plan); with
+ *                  K split, the cluster's reduction quantizes whole
+ *                  128-column groups, one warp each.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE (also N % 128 != 0), MISALIGNED,
  * FORMAT, CUDA, DEVICE.
  */
@@ -245,27 +246,19 @@ bfq_status bfq_gemm_block_fp8_quant(const void* a_q, const void* a_scales, int32
  * framework that owns all device memory, and serving loops that forbid
  * allocation after start-up because cudaMalloc can synchronize the device.
  * This entry point takes the same arguments as bfq_gemm_block_fp8 minus the
- * workspace and computes the same result with the same launch plan; its
- * split-K scratch is a static device array of bfq_gemm_noalloc_scratch_bytes()
- * (32 MiB) that every GPU loading the library holds until the process exits.
- *  - It allocates nothing and frees nothing (no cudaMalloc, no library
- *    allocator); inputs and outputs are still the caller's.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
- *  - All calls share the one array: calls that overlap on the GPU (different
- *    streams, or concurrent graph launches) race and corrupt each other.
- *    Serialize them.
- *  - A problem whose plan needs more scratch than the array holds returns
- *    BFQ_ERR_WORKSPACE and launches nothing.
- * Errors: those of bfq_gemm_block_fp8, plus WORKSPACE.
+ * workspace and computes the same result with the same launch plan.  No plan
+ * needs scratch (K splits reduce through distributed shared memory), so it
+ * allocates nothing, frees nothing and holds no device memory of its own;
+ * calls may overlap on the GPU like any other.  Inputs and outputs are the
+ * caller's.
+ * Errors: those of bfq_gemm_block_fp8.
  */
 bfq_status bfq_gemm_block_fp8_noalloc(const void* a_q, const void* a_scales, int32_t a_fmt,
                                       int64_t a_scale_ld, const void* w_q,
                                       const float* w_scales, int64_t M, int64_t N, int64_t K,
                                       void* out, void* stream);
 
-/* Size in bytes of the static scratch array of bfq_gemm_block_fp8_noalloc. */
+/* Device scratch held by bfq_gemm_block_fp8_noalloc, in bytes: 0. */
 size_t bfq_gemm_noalloc_scratch_bytes(void);
 
 /*

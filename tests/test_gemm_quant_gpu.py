@@ -30,37 +30,33 @@ def _problem(orc, bfq, M, N, K, a_fmt, seed):
     return (aq, sa, wq, sw), (d_aq, d_sa, d_wq, d_sw)
 
 
-def _fused(bfq, d, a_fmt, M, N, q_fmt, ld, with_out=True, split=True):
-    """split: pass the workspace the plain GEMM would use (K split over a
-    cluster where the plan splits); otherwise none (one CTA per tile)."""
-    K = d[0].shape[1]
+def _fused(bfq, d, a_fmt, M, N, q_fmt, ld, with_out=True):
     out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda") if with_out else None
     q = torch.full((M, N), 0x7E, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
     sc = torch.full((bfq.scale_cols(N, q_fmt), ld), SENT, dtype=torch.int32, device="cuda")
-    nbytes = bfq.bfq_gemm_workspace_bytes(M, N, K) if split else 0
-    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda") if nbytes else None
     bfq.bfq_gemm_block_fp8_quant(d[0], d[1], a_fmt, d[1].shape[-1], d[2], d[3], out, q_fmt, q, sc,
-                                 ld, workspace=ws)
+                                 ld)
     torch.cuda.synchronize()
     return out, q, sc
 
 
 # (M, N, K): ragged tiles, packed scale words left partial (N/128 = 1, 3,
-# 10), 128-wide tiles (N = 128), shapes the plain GEMM splits along K, and
-# enough tiles for the persistent schedule.
+# 10), 128-wide tiles (N = 128), shapes the plain GEMM splits along K
+# (through distributed shared memory), one CTA per 128-wide tile (100 x
+# 16384) and per 256-wide tile (1024 x 2560), and enough tiles for the
+# persistent schedule.
 SHAPES = [(40, 384, 1024), (64, 128, 512), (130, 512, 640), (257, 1280, 384), (24, 512, 4096),
-          (100, 16384, 256), (2048, 2560, 256)]
+          (100, 16384, 256), (1024, 2560, 512), (2048, 2560, 256)]
 
 
-@pytest.mark.parametrize("split", [True, False])
 @pytest.mark.parametrize("q_fmt", [0, 1, 2])
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_fused_output_quant_matches_quant_of_output(cuda_lib, orc, q_fmt, M, N, K, split):
+def test_fused_output_quant_matches_quant_of_output(cuda_lib, orc, q_fmt, M, N, K):
     bfq = cuda_lib
     a_fmt = 2 if q_fmt == 2 else 0
     (aq, sa, wq, sw), d = _problem(orc, bfq, M, N, K, a_fmt, seed=M + N + K + q_fmt)
     ld = bfq.align4(M) + 4
-    out, q, sc = _fused(bfq, d, a_fmt, M, N, q_fmt, ld, split=split)
+    out, q, sc = _fused(bfq, d, a_fmt, M, N, q_fmt, ld)
     # the bf16 output: within the GEMM tolerance of the oracle (sampled rows
     # for the large shape)
     rows = np.arange(M) if M <= 300 else np.unique(np.r_[0, M - 1, np.arange(5, M, 97)])

@@ -1,13 +1,12 @@
 """bfq_gemm_block_fp8_noalloc: the GEMM for callers that cannot allocate device
 memory (graph capture in global mode, frameworks that own all device memory,
-serving loops that forbid allocation after start-up).  Its split-K scratch is
-a static device array inside the library instead of a caller workspace.
+serving loops that forbid allocation after start-up).  No launch plan needs
+scratch (K splits reduce through distributed shared memory).
 
-The test calls it through the C ABI twice in a row on shapes whose launch
-plan splits K (so the scratch is really used, and the second call sees what
-the first left behind) and compares each result with the regular entry
-point's output on the same inputs, within the GEMM tolerance of the other
-tests.  This file is collected last so a failure here cannot hide others."""
+The test calls it through the C ABI twice in a row, on shapes whose launch
+plan splits K and on one that does not, and compares each result with the
+regular entry point's output on the same inputs, within the GEMM tolerance
+of the other tests.  This file is collected last so a failure here cannot hide others."""
 import ctypes
 
 import numpy as np
@@ -25,7 +24,7 @@ pytestmark = pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point(cuda_lib, orc, M, N, K, fmt):
     bfq = cuda_lib
     lib = bfq.load_library()
-    assert lib.bfq_gemm_noalloc_scratch_bytes() >= bfq.bfq_gemm_workspace_bytes(M, N, K)
+    assert lib.bfq_gemm_noalloc_scratch_bytes() == 0 == bfq.bfq_gemm_workspace_bytes(M, N, K)
     x = synth.activation(M, K, seed=M + N + K)
     w = synth.weight(N, K, seed=M + N + K + 1)
     aq, sa = orc.quant(bits(x), fmt)
@@ -35,7 +34,7 @@ def test_noalloc_matches_workspace_entry_point(cuda_lib, orc, M, N, K, fmt):
     d_wq = torch.from_numpy(wq).cuda().view(torch.float8_e4m3fn)
     d_sw = torch.from_numpy(sw).cuda()
 
-    ref = bfq.gemm(d_aq, d_sa, fmt, d_wq, d_sw)  # regular entry point, caller workspace
+    ref = bfq.gemm(d_aq, d_sa, fmt, d_wq, d_sw)  # regular entry point
     torch.cuda.synchronize()
     ref_h = ref.float().cpu().numpy().astype(np.float64)
     an = np.linalg.norm(orc.dequant_rows(aq, sa, fmt), axis=1)
