@@ -1135,6 +1135,15 @@ Plan dense_plan(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K) {
   if (pl.bn == 256 && pl.splits == 1 && pl.m_tiles * pl.n_tiles > dev.sm_count &&
       dev.smem_optin >= PersistCfg::kSmemBytes)
     pl.persist = true;
+  // Between one and 1.5 waves of long-K tiles (the persistent schedule would
+  // leave most SMs idle in its second round): K split two ways over 2-CTA
+  // clusters instead, 2 x tiles half-length CTAs in about three half-waves.
+  const int tiles = pl.m_tiles * pl.n_tiles;
+  if (pl.persist && tiles < 2 * dev.sm_count && tiles % dev.sm_count <= dev.sm_count / 2 &&
+      K / kBK >= 64 && max_active_clusters<256>(dev, 2) > 0) {
+    pl.persist = false;
+    pl.splits = 2;
+  }
   return pl;
 }
 
