@@ -901,13 +901,9 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
       }
-      // Every epilogue warp takes the same decision (the dense store and the
-      // fused silu-mul-quant below synchronise them on named barriers).
-      if (MASKED && !SILU) {
-        if (stop || *abort_flag) break;
-      } else if (named_barrier_or(2, C::kEpiWarps * 32, stop || *abort_flag)) {
-        break;
-      }
+      // Every epilogue warp takes the same decision (the stores and the fused
+      // silu-mul-quant below synchronise them on named barriers).
+      if (named_barrier_or(2, C::kEpiWarps * 32, stop || *abort_flag)) break;
 
       if constexpr (SILU) {
         // Fused silu(gate) * up + 1 x 128 group quant of the features of this
@@ -974,15 +970,35 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
           }
         }
       } else if (MASKED) {
-        if (warp_active && row_ok) {
-          __nv_bfloat16* dst = p.out + (int64_t)e * p.out_estride + (int64_t)m * p.N + col0;
+        // Rows past the count must not be written, so no TMA store: each
+        // 128 x 64 box is staged in shared memory (128-byte swizzle, as for
+        // dense tiles) and its valid rows are copied out with 16-byte stores,
+        // eight lanes per 128-byte row segment, so one store instruction
+        // writes four whole segments instead of 16 bytes of 32 rows.
+        const int rows_valid = min(kBM, m_limit - m0);
+        const int tid = (int)threadIdx.x - C::kEpiWarp0 * 32;
+        for (int blk = 0; blk < BN / 64; ++blk) {
+          named_barrier(1, C::kEpiWarps * 32);
+          if (half == (blk >> 1) && warp_active) {
+            const uint32_t row_addr = smem_u32(stg) + (uint32_t)(row_local * 128);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            if (c * 8 < ncols) {
-              const float2 f0 = unpack2(acc[c * 4 + 0]), f1 = unpack2(acc[c * 4 + 1]);
-              const float2 f2 = unpack2(acc[c * 4 + 2]), f3 = unpack2(acc[c * 4 + 3]);
-              st_v4(dst + c * 8, make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
-                                            pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
+            for (int c = 0; c < 8; ++c) {
+              const int a = (blk & 1) * 32 + c * 4;
+              const float2 f0 = unpack2(acc[a + 0]), f1 = unpack2(acc[a + 1]);
+              const float2 f2 = unpack2(acc[a + 2]), f3 = unpack2(acc[a + 3]);
+              st_shared_v4(row_addr + (uint32_t)((c ^ (row_local & 7)) << 4),
+                           make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
+                                      pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
+            }
+          }
+          named_barrier(1, C::kEpiWarps * 32);
+          if (n0 + blk * 64 < p.N) {
+            __nv_bfloat16* base =
+                p.out + (int64_t)e * p.out_estride + (int64_t)m0 * p.N + n0 + blk * 64;
+            for (int q = tid; q < rows_valid * 8; q += C::kEpiWarps * 32) {
+              const int r = q >> 3, c = q & 7;
+              st_v4(base + (int64_t)r * p.N + c * 8,
+                    ld_shared_v4(smem_u32(stg) + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4))));
             }
           }
         }
