@@ -575,11 +575,22 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
 // ----------------------------------------------------------------------------
 constexpr int kPersistMaxExperts = 1024;
 
-struct PersistCfg {
+// STAGES: depth of the operand ring.  The shared memory a fourth stage would
+// take holds three more output boxes instead, so the staging buffer holds one
+// 128-row x 64-column bf16 box (4 stages: the masked forms) or the whole
+// 128 x 256 tile (3 stages: dense tiles, whose four TMA stores then run on
+// while the next tile is promoted, instead of each box waiting for the last
+// to leave the buffer); the total is the same.
+template <int STAGES>
+struct PersistCfgT {
   using C = GemmCfg<256>;
-  static constexpr int kStagingBytes = kBM * 64 * 2;  // one 128-row x 64-column bf16 box
+  static_assert(STAGES == 3 || STAGES == 4, "3 or 4 operand stages");
+  static constexpr int kStages = STAGES;
+  static constexpr int kBoxBytes = kBM * 64 * 2;  // one 128-row x 64-column bf16 box
+  static constexpr int kStagingBoxes = STAGES == 4 ? 1 : 4;
+  static constexpr int kStagingBytes = kStagingBoxes * kBoxBytes;
   static constexpr int kPrefixBytes = (2 * kPersistMaxExperts + 2) * 4;
-  static constexpr size_t kSmemBytes = (size_t)C::kStages * C::kStageBytes + kStagingBytes +
+  static constexpr size_t kSmemBytes = (size_t)kStages * C::kStageBytes + kStagingBytes +
                                        C::kScaleBytes + kPrefixBytes + C::kBarrierBytes + 1024;
   // Register split of the 384-thread launch (168 each): warpgroup 0 keeps 40
   // (its tile walk spills at 24, which slowed every K block by ~30 %), the
@@ -588,6 +599,8 @@ struct PersistCfg {
   static constexpr int kEpiRegs = 232;
   static_assert(128 * kWg0Regs + 256 * kEpiRegs <= 384 * 168, "register split");
 };
+using PersistCfg = PersistCfgT<4>;
+static_assert(PersistCfgT<3>::kSmemBytes == PersistCfgT<4>::kSmemBytes, "same footprint");
 
 // Tile t of the persistent schedule -> (expert, first row, first column,
 // valid rows of the expert).  Masked: tpre[e] = tiles of experts < e,
@@ -619,20 +632,20 @@ __device__ __forceinline__ void persist_tile(int t, const GemmParams& p, const i
   }
 }
 
-template <bool MASKED, bool QOUT = false, bool SILU = false>
+template <bool MASKED, bool QOUT = false, bool SILU = false, int STAGES = 4>
 __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
     gemm_block_fp8_persistent(const __grid_constant__ CUtensorMap tmA,
                               const __grid_constant__ CUtensorMap tmW,
                               const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   constexpr int BN = 256;
   using C = GemmCfg<BN>;
-  using PC = PersistCfg;
+  using PC = PersistCfgT<STAGES>;
   static_assert(!SILU || (MASKED && !QOUT), "the fused silu-mul-quant output is a masked form");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
-  uint8_t* sB = smem + C::kStages * C::kABytes;
-  uint8_t* stg = smem + (size_t)C::kStages * C::kStageBytes;  // 1024-byte aligned
+  uint8_t* sB = smem + PC::kStages * C::kABytes;
+  uint8_t* stg = smem + (size_t)PC::kStages * C::kStageBytes;  // 1024-byte aligned
   uint32_t* sc_a = (uint32_t*)(stg + PC::kStagingBytes);       // [slot][128]
   uint32_t* sc_w = sc_a + C::kScaleSlots * kBM;                // [slot][2]
   int* tpre = (int*)(sc_w + 2 * C::kScaleSlots);               // [E + 1]
@@ -719,7 +732,7 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
   const int my_tiles =
       (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int steps = my_tiles * KB;
-  static_assert((C::kStages & (C::kStages - 1)) == 0 && C::kStages == 4, "ring of 4 stages");
+  static_assert(PC::kStages <= C::kStages, "barrier slots for the operand ring");
   static_assert(C::kScaleSlots == 8, "scale ring of 8 slots");
 
   if (warp < C::kEpiWarp0) {
@@ -735,8 +748,8 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
             a_row = (MASKED ? e * p.M : 0) + m0;
             w_row = (MASKED ? e * p.N : 0) + n0;
           }
-          const int s = g & 3;
-          const uint32_t ph = (uint32_t)(g >> 2) & 1u;
+          const int s = g % PC::kStages;
+          const uint32_t ph = (uint32_t)(g / PC::kStages) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
           mbar_arrive_expect_tx(&full[s], (uint32_t)C::kStageBytes);
           tma_load_2d_nohint(sA + (size_t)s * C::kABytes, &tmA, &full[s], i * kBK, a_row);
@@ -748,10 +761,10 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
         }
         if (*abort_flag) {
           // let the copies already issued land before the CTA can exit
-          for (int j = g - C::kStages < 0 ? 0 : g - C::kStages; j < g; ++j) {
+          for (int j = g - PC::kStages < 0 ? 0 : g - PC::kStages; j < g; ++j) {
             volatile int no_abort = 0;
-            (void)mbar_wait(&full[j & 3], (uint32_t)(j >> 2) & 1u, &no_abort, p.status,
-                            kWaitTimeoutNs / 8);
+            (void)mbar_wait(&full[j % PC::kStages], (uint32_t)(j / PC::kStages) & 1u, &no_abort,
+                            p.status, kWaitTimeoutNs / 8);
           }
         }
       }
@@ -761,13 +774,14 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
         constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
         int g = 0;
         for (; g < steps; ++g) {
-          const int s = g & 3;
+          const int s = g % PC::kStages;
           const int buf = g & 1;
           if (!mbar_wait(&tempty[buf], ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag, p.status,
                          kWaitTimeoutNs))
             break;
           tc_fence_after_sync();
-          if (!mbar_wait(&full[s], (uint32_t)(g >> 2) & 1u, abort_flag, p.status, kWaitTimeoutNs))
+          if (!mbar_wait(&full[s], (uint32_t)(g / PC::kStages) & 1u, abort_flag, p.status,
+                         kWaitTimeoutNs))
             break;
           tc_fence_after_sync();
           const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + (size_t)s * C::kABytes));
@@ -843,6 +857,27 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
       const int ncols = min(128, p.N - col0);
 
       uint64_t acc[64];
+      // Stages output boxes r0 .. r0 + kStagingBoxes - 1 of the tile (box b =
+      // columns b*64 .. b*64+63, held by warp half b/2) as bf16 in the 128-byte
+      // swizzled layout: 16-byte chunk c of row r at chunk c ^ (r mod 8).
+      auto stage_boxes = [&](int r0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int b = half * 2 + j;
+          if (b < r0 || b >= r0 + PC::kStagingBoxes || !warp_active || j * 64 >= ncols) continue;
+          const uint32_t row_addr =
+              smem_u32(stg) + (uint32_t)((b - r0) * PC::kBoxBytes + row_local * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int a = j * 32 + c * 4;  // pair index of column j*64 + c*8 of this half
+            const float2 f0 = unpack2(acc[a + 0]), f1 = unpack2(acc[a + 1]);
+            const float2 f2 = unpack2(acc[a + 2]), f3 = unpack2(acc[a + 3]);
+            st_shared_v4(row_addr + (uint32_t)((c ^ (row_local & 7)) << 4),
+                         make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
+                                    pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
+          }
+        }
+      };
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = 0ull;
       bool stop = false;
@@ -977,57 +1012,42 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
         // writes four whole segments instead of 16 bytes of 32 rows.
         const int rows_valid = min(kBM, m_limit - m0);
         const int tid = (int)threadIdx.x - C::kEpiWarp0 * 32;
-        for (int blk = 0; blk < BN / 64; ++blk) {
+        for (int r0 = 0; r0 < BN / 64; r0 += PC::kStagingBoxes) {
           named_barrier(1, C::kEpiWarps * 32);
-          if (half == (blk >> 1) && warp_active) {
-            const uint32_t row_addr = smem_u32(stg) + (uint32_t)(row_local * 128);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int a = (blk & 1) * 32 + c * 4;
-              const float2 f0 = unpack2(acc[a + 0]), f1 = unpack2(acc[a + 1]);
-              const float2 f2 = unpack2(acc[a + 2]), f3 = unpack2(acc[a + 3]);
-              st_shared_v4(row_addr + (uint32_t)((c ^ (row_local & 7)) << 4),
-                           make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
-                                      pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
-            }
-          }
+          stage_boxes(r0);
           named_barrier(1, C::kEpiWarps * 32);
-          if (n0 + blk * 64 < p.N) {
+          for (int b = r0; b < r0 + PC::kStagingBoxes; ++b) {
+            if (n0 + b * 64 >= p.N) break;
+            const uint32_t box = smem_u32(stg) + (uint32_t)((b - r0) * PC::kBoxBytes);
             __nv_bfloat16* base =
-                p.out + (int64_t)e * p.out_estride + (int64_t)m0 * p.N + n0 + blk * 64;
+                p.out + (int64_t)e * p.out_estride + (int64_t)m0 * p.N + n0 + b * 64;
             for (int q = tid; q < rows_valid * 8; q += C::kEpiWarps * 32) {
               const int r = q >> 3, c = q & 7;
               st_v4(base + (int64_t)r * p.N + c * 8,
-                    ld_shared_v4(smem_u32(stg) + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4))));
+                    ld_shared_v4(box + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4))));
             }
           }
         }
       } else {
-        // Four 128 x 64 boxes through the staging buffer (128-byte swizzle,
-        // 16-byte chunk c of row r at chunk c ^ (r mod 8)); rows >= M are
-        // clipped by the tensor map.  (Fused output quant: the bf16 output is
-        // optional; the condition is the same for every thread.)
-#pragma unroll
-        for (int blk = 0; blk < ((!QOUT || p.out != nullptr) ? BN / 64 : 0); ++blk) {
-          if (store_thread) bulk_wait_read_all();  // previous box has left the buffer
-          named_barrier(1, C::kEpiWarps * 32);
-          if (half == (blk >> 1) && warp_active) {
-            const uint32_t row_addr = smem_u32(stg) + (uint32_t)(row_local * 128);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int a = (blk & 1) * 32 + c * 4;  // pair index of column (blk&1)*64 + c*8
-              const float2 f0 = unpack2(acc[a + 0]), f1 = unpack2(acc[a + 1]);
-              const float2 f2 = unpack2(acc[a + 2]), f3 = unpack2(acc[a + 3]);
-              st_shared_v4(row_addr + (uint32_t)((c ^ (row_local & 7)) << 4),
-                           make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
-                                      pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
+        // The tile's four 128 x 64 boxes through the staging buffer, one at
+        // a time or all at once (3-stage ring); rows >= M are clipped by the
+        // tensor map.  The stores run on while the next tile is promoted;
+        // the buffer is only rewritten once they have read it.  (Fused output
+        // quant: the bf16 output is optional; the condition is the same for
+        // every thread.)
+        if (!QOUT || p.out != nullptr) {
+          for (int r0 = 0; r0 < BN / 64; r0 += PC::kStagingBoxes) {
+            if (store_thread) bulk_wait_read_all();  // earlier boxes have left the buffer
+            named_barrier(1, C::kEpiWarps * 32);
+            stage_boxes(r0);
+            fence_proxy_async_smem();
+            named_barrier(1, C::kEpiWarps * 32);
+            if (store_thread) {
+              for (int b = r0; b < r0 + PC::kStagingBoxes; ++b)
+                if (n0 + b * 64 < p.N)
+                  tma_store_2d(&tmO, stg + (b - r0) * PC::kBoxBytes, n0 + b * 64, m0);
+              bulk_commit();
             }
-          }
-          fence_proxy_async_smem();
-          named_barrier(1, C::kEpiWarps * 32);
-          if (store_thread && n0 + blk * 64 < p.N) {
-            tma_store_2d(&tmO, stg, n0 + blk * 64, m0);
-            bulk_commit();
           }
         }
         if constexpr (QOUT) {
@@ -1247,22 +1267,23 @@ Plan masked_plan(const DeviceInfo& dev, int64_t E, int64_t T, int64_t N, int64_t
   return pl;
 }
 
-template <bool MASKED, bool QOUT = false, bool SILU = false>
+template <bool MASKED, bool QOUT = false, bool SILU = false, int STAGES = 4>
 bfq_status configure_persistent(const DeviceInfo& dev) {
   static bool configured[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (configured[dev.ordinal]) return BFQ_OK;
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, gemm_block_fp8_persistent<MASKED, QOUT, SILU>) != cudaSuccess) {
+  if (cudaFuncGetAttributes(&fa, gemm_block_fp8_persistent<MASKED, QOUT, SILU, STAGES>) !=
+      cudaSuccess) {
     cudaGetLastError();
     return BFQ_ERR_CUDA;
   }
   // setmaxnreg.inc only completes if the launch allocation covers the split
   if (fa.numRegs != GemmCfg<256>::kLaunchRegs) return BFQ_ERR_DEVICE;
-  if (cudaFuncSetAttribute(gemm_block_fp8_persistent<MASKED, QOUT, SILU>,
+  if (cudaFuncSetAttribute(gemm_block_fp8_persistent<MASKED, QOUT, SILU, STAGES>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)PersistCfg::kSmemBytes) != cudaSuccess) {
+                           (int)PersistCfgT<STAGES>::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     return BFQ_ERR_CUDA;
   }
@@ -1270,15 +1291,24 @@ bfq_status configure_persistent(const DeviceInfo& dev) {
   return BFQ_OK;
 }
 
-template <bool MASKED, bool QOUT = false, bool SILU = false>
+template <bool MASKED, bool QOUT = false, bool SILU = false, int STAGES = 4>
 bfq_status launch_persistent(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
                              const CUtensorMap& mo, const GemmParams& p, unsigned grid,
                              cudaStream_t s) {
-  bfq_status st = configure_persistent<MASKED, QOUT, SILU>(dev);
+  bfq_status st = configure_persistent<MASKED, QOUT, SILU, STAGES>(dev);
   if (st != BFQ_OK) return st;
-  return launch_status(launch_pdl(gemm_block_fp8_persistent<MASKED, QOUT, SILU>, dim3(grid),
-                                  dim3(GemmCfg<256>::kThreads), PersistCfg::kSmemBytes, s, 1u, ma,
-                                  mw, mo, p));
+  return launch_status(launch_pdl(gemm_block_fp8_persistent<MASKED, QOUT, SILU, STAGES>,
+                                  dim3(grid), dim3(GemmCfg<256>::kThreads),
+                                  PersistCfgT<STAGES>::kSmemBytes, s, 1u, ma, mw, mo, p));
+}
+
+// Dense persistent launch: the 3-stage ring, so that the whole output tile is
+// staged at once and its four TMA stores overlap the next tile's promotion.
+template <bool QOUT>
+bfq_status launch_dense_persistent(const DeviceInfo& dev, const CUtensorMap& ma,
+                                   const CUtensorMap& mw, const CUtensorMap& mo,
+                                   const GemmParams& p, unsigned grid, cudaStream_t s) {
+  return launch_persistent<false, QOUT, false, 3>(dev, ma, mw, mo, p, grid, s);
 }
 
 bfq_status check_device(DeviceInfo* dev) {
@@ -1370,11 +1400,11 @@ bfq_status gemm_dense(const void* a_q, const void* a_scales, int32_t a_fmt, int6
   const unsigned pgrid = grid < (unsigned)dev.sm_count ? grid : (unsigned)dev.sm_count;
   cudaStream_t s = (cudaStream_t)stream;
   if (qo) {
-    if (pl.persist) return launch_persistent<false, true>(dev, ma, mw, mo, p, pgrid, s);
+    if (pl.persist) return launch_dense_persistent<true>(dev, ma, mw, mo, p, pgrid, s);
     return pl.bn == 256 ? launch<256, false, true>(dev, ma, mw, mo, p, grid, s)
                         : launch<128, false, true>(dev, ma, mw, mo, p, grid, s);
   }
-  if (pl.persist) return launch_persistent<false>(dev, ma, mw, mo, p, pgrid, s);
+  if (pl.persist) return launch_dense_persistent<false>(dev, ma, mw, mo, p, pgrid, s);
   return pl.bn == 256 ? launch<256, false>(dev, ma, mw, mo, p, grid, s)
                       : launch<128, false>(dev, ma, mw, mo, p, grid, s);
 }
