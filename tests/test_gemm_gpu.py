@@ -163,6 +163,32 @@ def test_gemm_parity_narrow_unsplit_plan(cuda_lib, orc, fmt, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", [0, 2])
+@pytest.mark.parametrize("M,N,K", [(1280, 4224, 8192)])
+def test_gemm_parity_two_way_split_for_a_partial_second_wave(cuda_lib, orc, fmt, M, N, K):
+    """170 tiles of 128 x 256 (the last column tile half full) with 64 K
+    blocks: between one and 1.5 waves on 152 SMs, so the plan splits K two
+    ways over 2-CTA clusters (340 half-length CTAs) instead of a persistent
+    second round.  Three sampled rows of every row tile, every column."""
+    bfq = cuda_lib
+    aq, sa, wq, sw = _oracle_problem(orc, M, N, K, fmt, seed=57 + fmt)
+    d = _to_dev(aq, sa, wq, sw, fmt)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bfq.gemm(d[0], d[1], fmt, d[2], d[3], out=out)
+    out2 = bfq.gemm(d[0], d[1], fmt, d[2], d[3])
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+    rng = np.random.default_rng(5 + fmt)
+    rows = np.unique(np.concatenate(
+        [[t * 128, min(M, t * 128 + 128) - 1, rng.integers(t * 128, min(M, t * 128 + 128))]
+         for t in range((M + 127) // 128)]))
+    ref = orc.gemm(aq, sa, fmt, wq, sw, rows=rows)
+    an, wn = _norms(orc, aq, sa, wq, sw, fmt, rows=rows)
+    got = out.float().cpu().numpy()
+    assert_gemm_close(got[rows], ref, an, wn, f"two-way split {M}x{N}x{K} fmt{fmt}")
+    assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("fmt", [0, 2])
 @pytest.mark.parametrize("M,N,K", [(2000, 8192, 256), (2048, 2432, 256), (1100, 5120, 256)])
 def test_gemm_parity_persistent_many_tiles(cuda_lib, orc, fmt, M, N, K):
     """More 256-wide tiles than SMs, so the persistent schedule walks several
