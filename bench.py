@@ -90,12 +90,20 @@ def load_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources' code: comments, trailing blanks and empty
+    lines are left out, so that a comment edit keeps the measured profile."""
+    import re
+
     h = hashlib.sha256()
     for rel in ("block_scaled_fp8_quant_gb300/csrc/gemm_kernels.cu",
                 "block_scaled_fp8_quant_gb300/csrc/bfq_device.cuh",
                 "block_scaled_fp8_quant_gb300/csrc/quant_kernels.cu"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        code = "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 

@@ -16,9 +16,14 @@
 //   warps 2..   epilogue ("promotion"): per K block, read the fp32 partial of
 //               its 32 rows x 128 columns from TMEM, multiply by the scale
 //               product sA[m, b] * sW[nblk, b] and accumulate in registers.
-//               At the end convert to bf16 and store the row, or (split-K)
-//               store fp32 partials; the last CTA of a tile to finish sums the
-//               splits in split order (deterministic) and stores bf16.
+//               At the end convert to bf16 and store the tile through shared
+//               memory, or (K split over a thread-block cluster) keep the
+//               fp32 partial in the CTA's shared memory; every CTA of the
+//               cluster then sums its slice of the tile over the splits, read
+//               through distributed shared memory in split order
+//               (deterministic), and stores bf16.
+// The persistent form (one CTA per SM walking many tiles) and the masked
+// per-expert forms are described at their kernel.
 // Every wait is bounded: a wait that gives up latches BFQ_ERR_TIMEOUT in the
 // library's status word, every role drains and the CTA frees its TMEM and
 // exits.
@@ -566,8 +571,10 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
 // issuer and the scale loader run ahead across tile boundaries, so a tile's
 // promotion drain and store overlap the next tile's loads and first MMAs, and
 // barrier and TMEM set-up are paid once per SM rather than once per tile.
-// Dense tiles leave through a dedicated 16 KB staging buffer, one 128 x 64
-// TMA-store box at a time (the stage ring stays busy with the next tile).
+// Tiles leave through a dedicated staging buffer (the stage ring stays busy
+// with the next tile): dense tiles stage the whole 128 x 256 tile and issue
+// its four TMA-store boxes together; masked tiles stage one 128 x 64 box at
+// a time and copy its valid rows out with coalesced stores.
 // Masked: the tile list holds only row tiles that start below their expert's
 // count — per-expert tile counts are prefix-summed in shared memory at start
 // — so padding costs no CTA time and the valid tiles spread evenly over the
