@@ -195,9 +195,9 @@ SAMPLE_COLS = 1024
 CPU_BASELINE_SECONDS = 10.0
 
 
-def oracle_sample_step():
+def oracle_sample_step(cols=SAMPLE_COLS):
     """One bounded sample of the workload on the CPU oracle: 8 activation rows
-    against the first 1024 weight rows of each of the 6 (n, k) shapes (weight
+    against the first `cols` weight rows of each of the 6 (n, k) shapes (weight
     block quant of that slice, activation quant, GEMM).  Returns FLOPs done."""
     import numpy as np
 
@@ -206,14 +206,14 @@ def oracle_sample_step():
 
     flops = 0
     for n, k in SWEEP_NK:
-        w = synth.weight(SAMPLE_COLS, k, seed=n + k)
+        w = synth.weight(cols, k, seed=n + k)
         x = synth.activation(SAMPLE_ROWS, k, seed=SAMPLE_ROWS * 31 + n)
         wb = w.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
         xb = x.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
         wq, sw = oracle.weight_block_quant(wb, False)
         aq, sa = oracle.quant(xb, oracle.FMT_F32)
         oracle.gemm(aq, sa, oracle.FMT_F32, wq, sw)
-        flops += 2 * SAMPLE_ROWS * SAMPLE_COLS * k
+        flops += 2 * SAMPLE_ROWS * cols * k
     return flops
 
 
@@ -240,12 +240,17 @@ def run_reference(args, rank, world):
     import oracle
 
     oracle.build_oracle()
+    # The weight-row sample shrinks with the number of steps so that the whole
+    # run stays near a minute and a half of CPU time (~2 s per step at 1024
+    # rows on the GPU machine's host cores).
+    cols = max(128, min(SAMPLE_COLS, SAMPLE_COLS * 40 // max(1, args.steps + args.warmup)
+                        // 128 * 128))
     for _ in range(args.warmup):
-        oracle_sample_step()
+        oracle_sample_step(cols)
     t0 = time.perf_counter()
     flops = 0
     for _ in range(args.steps):
-        flops += oracle_sample_step()
+        flops += oracle_sample_step(cols)
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
     line = {
@@ -254,7 +259,7 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "bounded CPU sample"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{SAMPLE_ROWS} rows x {SAMPLE_COLS} weight rows per (n,k), "
+                         "sample": f"{SAMPLE_ROWS} rows x {cols} weight rows per (n,k), "
                                    f"per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
