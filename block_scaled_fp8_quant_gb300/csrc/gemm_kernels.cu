@@ -247,8 +247,8 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
           mbar_arrive_expect_tx(&full[s], (uint32_t)C::kStageBytes);
           const int kx = (kb_begin + i) * kBK;
-          tma_load_2d_nohint(sA + (size_t)s * C::kABytes, &tmA, &full[s], kx, a_row);
-          tma_load_2d_nohint(sB + (size_t)s * C::kBBytes, &tmW, &full[s], kx, w_row);
+          tma_load_2d(sA + (size_t)s * C::kABytes, &tmA, &full[s], kx, a_row);
+          tma_load_2d(sB + (size_t)s * C::kBBytes, &tmW, &full[s], kx, w_row);
           ++issued;
         }
         if (*abort_flag) {
@@ -759,8 +759,8 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
           const uint32_t ph = (uint32_t)(g / PC::kStages) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
           mbar_arrive_expect_tx(&full[s], (uint32_t)C::kStageBytes);
-          tma_load_2d_nohint(sA + (size_t)s * C::kABytes, &tmA, &full[s], i * kBK, a_row);
-          tma_load_2d_nohint(sB + (size_t)s * C::kBBytes, &tmW, &full[s], i * kBK, w_row);
+          tma_load_2d(sA + (size_t)s * C::kABytes, &tmA, &full[s], i * kBK, a_row);
+          tma_load_2d(sB + (size_t)s * C::kBBytes, &tmW, &full[s], i * kBK, w_row);
           if (++i == KB) {
             i = 0;
             t += gridDim.x;
