@@ -163,12 +163,15 @@ def test_gemm_parity_narrow_unsplit_plan(cuda_lib, orc, fmt, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", [0, 2])
-@pytest.mark.parametrize("M,N,K", [(1280, 4224, 8192)])
+@pytest.mark.parametrize("M,N,K", [(1280, 4224, 8192), (1536, 4608, 4096)])
 def test_gemm_parity_two_way_split_for_a_partial_second_wave(cuda_lib, orc, fmt, M, N, K):
-    """170 tiles of 128 x 256 (the last column tile half full) with 64 K
-    blocks: between one and 1.5 waves on 152 SMs, so the plan splits K two
-    ways over 2-CTA clusters (340 half-length CTAs) instead of a persistent
-    second round.  Three sampled rows of every row tile, every column."""
+    """A last wave at most half full.  1280 x 4224 x 8192: 170 tiles of
+    128 x 256 (the last column tile half full) with 64 K blocks, so every
+    tile's K is split two ways over 2-CTA clusters (340 half-length CTAs)
+    instead of a persistent second round.  1536 x 4608 x 4096: 216 tiles
+    with 32 K blocks, too short a K for that split, so the persistent kernel
+    walks them in two rounds, the second 64 tiles long.  Three sampled rows
+    of every row tile, every column."""
     bfq = cuda_lib
     aq, sa, wq, sw = _oracle_problem(orc, M, N, K, fmt, seed=57 + fmt)
     d = _to_dev(aq, sa, wq, sw, fmt)
