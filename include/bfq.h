@@ -75,7 +75,7 @@ enum {
   BFQ_ERR_FORMAT = 4,            /* scale format not allowed for this operand  */
   BFQ_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed          */
   BFQ_ERR_TIMEOUT = 6,           /* a kernel watchdog gave up waiting          */
-  BFQ_ERR_WORKSPACE = 7,         /* workspace too small (kept for ABI stability; no current plan needs one) */
+  BFQ_ERR_WORKSPACE = 7,         /* unused: no current plan needs a workspace  */
   BFQ_ERR_DEVICE = 8             /* current device is not sm_100 family        */
 };
 
