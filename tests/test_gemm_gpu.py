@@ -192,13 +192,15 @@ def test_gemm_parity_two_way_split_for_a_partial_second_wave(cuda_lib, orc, fmt,
 
 
 @pytest.mark.parametrize("fmt", [0, 2])
-@pytest.mark.parametrize("M,N,K", [(2000, 8192, 256), (2048, 2432, 256), (1100, 5120, 256)])
+@pytest.mark.parametrize("M,N,K", [(2000, 8192, 256), (2048, 2432, 256), (2048, 2496, 256),
+                                   (1100, 5120, 256)])
 def test_gemm_parity_persistent_many_tiles(cuda_lib, orc, fmt, M, N, K):
     """More 256-wide tiles than SMs, so the persistent schedule walks several
     tiles per SM.  2000 x 8192: 16 row tiles, the last one ragged, x 32
-    column tiles; 2048 x 2432: the last column tile half full; 1100 x 5120:
-    an odd number of row tiles.  Three sampled rows of every row tile against
-    the oracle, every column."""
+    column tiles; 2048 x 2432 and 2048 x 2496: the last column tile half and
+    three quarters full (two and three of its four staged output boxes
+    stored); 1100 x 5120: an odd number of row tiles.  Three sampled rows of
+    every row tile against the oracle, every column."""
     bfq = cuda_lib
     assert bfq.bfq_gemm_workspace_bytes(M, N, K) == 0
     aq, sa, wq, sw = _oracle_problem(orc, M, N, K, fmt, seed=31 + fmt + N)

@@ -44,12 +44,12 @@ def _fused(bfq, d, a_fmt, M, N, q_fmt, ld, with_out=True):
 # 10, 19, 33), 128-wide tiles (N = 128), shapes the plain GEMM splits along
 # K (through distributed shared memory), one CTA per 128-wide tile (100 x
 # 16384) and per 256-wide tile (1024 x 2560), the persistent schedule (with
-# a half-full last column tile at 2048 x 2432, and a second round of 64
-# tiles at 1536 x 4608 x 4096), and the two-way split of a partial second
-# wave (1280 x 4224 x 8192).
+# a half-full last column tile at 2048 x 2432, a second round of 64 tiles at
+# 1536 x 4608 x 4096, and a ragged last row tile at 2000 x 2560), and the
+# two-way split of a partial second wave (1280 x 4224 x 8192).
 SHAPES = [(40, 384, 1024), (64, 128, 512), (130, 512, 640), (257, 1280, 384), (24, 512, 4096),
           (100, 16384, 256), (1024, 2560, 512), (2048, 2560, 256), (2048, 2432, 384),
-          (1280, 4224, 8192), (1536, 4608, 4096)]
+          (1280, 4224, 8192), (1536, 4608, 4096), (2000, 2560, 256)]
 
 
 @pytest.mark.parametrize("q_fmt", [0, 1, 2])
