@@ -308,21 +308,49 @@ def step(bfq, shapes, events=None):
 
 
 class E2EPipeline:
-    """End-to-end step through the public API with host buffers: for every
-    shape, copy its activations host->device, quantize, run the GEMM and copy
-    the result device->host.  Three streams overlap the transfers of one shape
-    with the compute of its neighbours; CUDA events order each shape's
-    copy-in -> compute -> copy-out and keep device buffers from being reused
-    before the copy that reads them has finished."""
+    """End-to-end step through the public API with host buffers: the shapes
+    of one (n, k) weight share one pinned host input buffer, one device input
+    buffer, one device output buffer and one pinned host output buffer, so
+    every step copies each group's activations host->device in one copy,
+    quantizes and multiplies every shape of the group, and copies the
+    group's results device->host in one copy.  Three streams overlap the
+    transfers of one group with the compute of its neighbours; CUDA events
+    order each group's copy-in -> compute -> copy-out and keep device buffers
+    from being reused before the copy that reads them has finished."""
 
-    def __init__(self, torch, shapes, host_x, host_out):
+    def __init__(self, torch, shapes):
         self.torch = torch
-        self.shapes = shapes
-        self.host_x = host_x
-        self.host_out = host_out
+        self.groups = []
+        i = 0
+        while i < len(shapes):
+            j = i
+            while j < len(shapes) and (shapes[j]["n"], shapes[j]["k"]) == (shapes[i]["n"],
+                                                                           shapes[i]["k"]):
+                j += 1
+            grp = shapes[i:j]
+            n_in = sum(s["x"].numel() for s in grp)
+            n_out = sum(s["out"].numel() for s in grp)
+            dev = grp[0]["x"].device
+            g = dict(shapes=grp,
+                     d_in=torch.empty(n_in, dtype=torch.bfloat16, device=dev),
+                     d_out=torch.empty(n_out, dtype=torch.bfloat16, device=dev),
+                     h_in=torch.empty(n_in, dtype=torch.bfloat16).pin_memory(),
+                     h_out=torch.empty(n_out, dtype=torch.bfloat16).pin_memory(),
+                     xs=[], outs=[])
+            a = b = 0
+            for s in grp:
+                n1, n2 = s["x"].numel(), s["out"].numel()
+                g["h_in"][a:a + n1].copy_(s["x"].reshape(-1).cpu())
+                g["xs"].append(g["d_in"][a:a + n1].view(s["x"].shape))
+                g["outs"].append(g["d_out"][b:b + n2].view(s["out"].shape))
+                a, b = a + n1, b + n2
+            self.groups.append(g)
+            i = j
+        self.h2d_bytes = sum(g["h_in"].numel() * 2 for g in self.groups)
+        self.d2h_bytes = sum(g["h_out"].numel() * 2 for g in self.groups)
         self.s_in = torch.cuda.Stream()
         self.s_out = torch.cuda.Stream()
-        n = len(shapes)
+        n = len(self.groups)
         self.ev_in = [torch.cuda.Event() for _ in range(n)]
         self.ev_done = [torch.cuda.Event() for _ in range(n)]
         self.ev_out = [torch.cuda.Event() for _ in range(n)]
@@ -331,22 +359,23 @@ class E2EPipeline:
     def step(self, bfq):
         torch = self.torch
         comp = torch.cuda.current_stream()
-        for i, (sh, hx, ho) in enumerate(zip(self.shapes, self.host_x, self.host_out)):
+        for i, g in enumerate(self.groups):
             with torch.cuda.stream(self.s_in):
-                if not self.first:  # x of this shape is free once last step's quant ran
+                if not self.first:  # the inputs are free once last step's group ran
                     self.s_in.wait_event(self.ev_done[i])
-                sh["x"].copy_(hx, non_blocking=True)
+                g["d_in"].copy_(g["h_in"], non_blocking=True)
                 self.ev_in[i].record()
             comp.wait_event(self.ev_in[i])
-            if not self.first:  # out of this shape is free once last step copied it
+            if not self.first:  # the outputs are free once last step copied them
                 comp.wait_event(self.ev_out[i])
-            bfq.bfq_quant(sh["x"], sh["q"], sh["s"], bfq.SCALE_F32, sh["s"].shape[-1])
-            bfq.bfq_gemm_block_fp8(sh["q"], sh["s"], bfq.SCALE_F32, sh["s"].shape[-1], sh["wq"],
-                                   sh["sw"], sh["out"], sh["ws"])
+            for sh, x, out in zip(g["shapes"], g["xs"], g["outs"]):
+                bfq.bfq_quant(x, sh["q"], sh["s"], bfq.SCALE_F32, sh["s"].shape[-1])
+                bfq.bfq_gemm_block_fp8(sh["q"], sh["s"], bfq.SCALE_F32, sh["s"].shape[-1],
+                                       sh["wq"], sh["sw"], out, sh["ws"])
             self.ev_done[i].record(comp)
             with torch.cuda.stream(self.s_out):
                 self.s_out.wait_event(self.ev_done[i])
-                ho.copy_(sh["out"], non_blocking=True)
+                g["h_out"].copy_(g["d_out"], non_blocking=True)
                 self.ev_out[i].record()
         self.first = False
 
@@ -710,11 +739,8 @@ def run_gpu(args, rank, world, local_rank):
                          gemm_alg_bytes(s["m"], s["n"], s["k"]) / (hbm_peak * 1e9)) for s in shapes)
 
     # end to end through the public API with host buffers (pinned)
-    host_x = [s["x"].cpu().pin_memory() for s in shapes]
-    host_out = [torch.empty(s["out"].shape, dtype=torch.bfloat16).pin_memory() for s in shapes]
-    h2d = sum(x.numel() * 2 for x in host_x)
-    d2h = sum(o.numel() * 2 for o in host_out)
-    pipe = E2EPipeline(torch, shapes, host_x, host_out)
+    pipe = E2EPipeline(torch, shapes)
+    h2d, d2h = pipe.h2d_bytes, pipe.d2h_bytes
     for _ in range(max(1, args.warmup)):
         pipe.step(bfq)
     pipe.join()
@@ -753,9 +779,10 @@ def run_gpu(args, rank, world, local_rank):
         "e2e": {"value": world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.steps,
-                "how": "public C-ABI calls per shape; pinned host buffers; H2D, compute and "
-                       "D2H on three streams ordered by events (transfers of one shape "
-                       "overlap its neighbours' compute)"},
+                "how": "public C-ABI calls per shape; pinned host buffers, one H2D and one "
+                       "D2H per (n,k) group of shapes; H2D, compute and D2H on three streams "
+                       "ordered by events (transfers of one group overlap its neighbours' "
+                       "compute)"},
         "gpu_launches": 2 * n_shapes * args.steps,
         "roofline": {"bound": "tensor", "achieved": round(achieved_tflops, 1),
                      "peak": fp8_peak, "unit": "TFLOP/s",
