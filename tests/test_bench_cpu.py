@@ -43,3 +43,24 @@ def test_reference_arm_other_ranks_do_nothing():
              "--warmup", "0")
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_kernel_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    """The committed DRAM-traffic profile is tied to the kernels' code: a
+    comment edit keeps its hash, a code edit changes it."""
+    import shutil
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    csrc = tmp_path / "block_scaled_fp8_quant_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("gemm_kernels.cu", "bfq_device.cuh", "quant_kernels.cu"):
+        shutil.copy(os.path.join(ROOT, "block_scaled_fp8_quant_gb300", "csrc", f), csrc / f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    g = csrc / "gemm_kernels.cu"
+    g.write_text(g.read_text() + "\n// a comment\n/* another\n   comment */\n\n")
+    assert bench.kernel_source_hash() == h0
+    g.write_text(g.read_text() + "static const int kUnusedForTheTest = 1;\n")
+    assert bench.kernel_source_hash() != h0
