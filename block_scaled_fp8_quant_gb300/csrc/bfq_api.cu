@@ -7,6 +7,8 @@
 namespace bfq {
 
 __device__ int g_device_status = 0;
+// Where take_status_kernel leaves the value it took from the latch.
+__device__ int g_status_taken = 0;
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -81,6 +83,11 @@ __global__ void watchdog_selftest_kernel(int* status, uint64_t timeout_ns) {
   __syncthreads();
 }
 
+// Reads and clears the latch in one atomic exchange, so that a timeout a
+// kernel on another stream latches at the same moment is either returned now
+// or kept for the next poll, never lost between a read and a clear.
+__global__ void take_status_kernel(int* status, int* taken) { *taken = atomicExch(status, 0); }
+
 }  // namespace bfq
 
 using namespace bfq;
@@ -104,12 +111,16 @@ extern "C" const char* bfq_status_string(bfq_status status) {
 
 extern "C" bfq_status bfq_poll_device_status(void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
+  int* status = device_status_ptr();
+  int* taken = nullptr;
+  if (!status || cudaGetSymbolAddress((void**)&taken, g_status_taken) != cudaSuccess) {
+    cudaGetLastError();
+    return BFQ_ERR_CUDA;
+  }
   int host = 0;
-  const int zero = 0;
-  if (cudaMemcpyFromSymbolAsync(&host, g_device_status, sizeof(int), 0,
-                                cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
-                              s) != cudaSuccess ||
+  take_status_kernel<<<1, 1, 0, s>>>(status, taken);
+  if (cudaGetLastError() != cudaSuccess ||
+      cudaMemcpyAsync(&host, taken, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {
     cudaGetLastError();
     return BFQ_ERR_CUDA;

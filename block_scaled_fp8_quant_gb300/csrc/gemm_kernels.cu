@@ -1500,11 +1500,10 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked(
 // ----------------------------------------------------------------------------
 // Entry point that allocates nothing.
 //
-// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is
-// captured in global mode (allocation is an error there), plugins inside a
-// host framework that owns every byte of device memory, and serving loops
-// that forbid allocation after start-up because cudaMalloc can synchronize
-// the device.  The K splits reduce through distributed shared memory, so no
+// Some callers cannot call cudaMalloc: plugins inside a host framework that
+// owns every byte of device memory through its own allocator, and serving
+// loops that forbid allocation after start-up because cudaMalloc can
+// synchronize the device.  The K splits reduce through distributed shared memory, so no
 // plan needs scratch: this is the regular call without a workspace.
 // ----------------------------------------------------------------------------
 extern "C" size_t bfq_gemm_noalloc_scratch_bytes(void) { return 0; }

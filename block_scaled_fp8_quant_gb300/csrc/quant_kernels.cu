@@ -291,7 +291,10 @@ extern "C" bfq_status bfq_quant(const void* x, int64_t M, int64_t K, int64_t ld_
   if (group != 128 || K % 128 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
   if (M == 0) return BFQ_OK;
   if (!x || !q || !scales) return BFQ_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || ld_x % 8 != 0)
+  // scale_ld % 4: each scale column starts on a 16-byte boundary, the layout
+  // the GEMM's activation-scale argument requires
+  if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || ld_x % 8 != 0 ||
+      scale_ld % 4 != 0)
     return BFQ_ERR_MISALIGNED;
   DeviceInfo dev;
   bfq_status st = current_device(&dev);
@@ -334,7 +337,8 @@ extern "C" bfq_status bfq_silu_mul_quant(const void* x, int32_t E, int32_t T, in
   if (I % 128 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
   if (E == 0 || T == 0) return BFQ_OK;
   if (!x || !valid_counts || !q || !scales) return BFQ_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(q) || !aligned16(scales)) return BFQ_ERR_MISALIGNED;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || scale_ld % 4 != 0)
+    return BFQ_ERR_MISALIGNED;
   if (E > 65535) return BFQ_ERR_UNSUPPORTED_SHAPE;
   DeviceInfo dev;
   bfq_status st = current_device(&dev);

@@ -108,8 +108,9 @@ const char* bfq_status_string(bfq_status status);
  *   group    must be 128.
  *   fmt      a bfq_scale_fmt.
  *   q        e4m3 [M][K] (row stride K), 16-byte aligned.
- *   scales   column-major, see the header comment; scale_ld >= M.  Entries of
- *            rows >= M are not written.
+ *   scales   column-major, see the header comment, 16-byte aligned;
+ *            scale_ld >= M and scale_ld % 4 == 0 (the TMA-aligned layout the
+ *            GEMM takes).  Entries of rows >= M are not written.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
  */
 bfq_status bfq_quant(const void* x, int64_t M, int64_t K, int64_t ld_x, int32_t group,
@@ -135,7 +136,8 @@ bfq_status bfq_quant(const void* x, int64_t M, int64_t K, int64_t ld_x, int32_t 
  *   fmt           a bfq_scale_fmt.
  *   q             e4m3 [E][T][I], 16-byte aligned.
  *   scales        [E][cols][scale_ld], cols = I/128 (fp32 formats) or
- *                 ceil(I/512) (packed), scale_ld >= T.
+ *                 ceil(I/512) (packed), 16-byte aligned, scale_ld >= T,
+ *                 scale_ld % 4 == 0.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
  */
 bfq_status bfq_silu_mul_quant(const void* x, int32_t E, int32_t T, int32_t I,
@@ -241,10 +243,11 @@ bfq_status bfq_gemm_block_fp8_quant(const void* a_q, const void* a_scales, int32
  * bfq_gemm_block_fp8 for callers that cannot allocate device memory.  (The
  * pages have no counterpart; this is a convenience of this library.)
  *
- * Some callers cannot call cudaMalloc: code running while a CUDA graph is
- * captured in global mode (allocation is an error there), plugins inside a
- * framework that owns all device memory, and serving loops that forbid
- * allocation after start-up because cudaMalloc can synchronize the device.
+ * Some callers cannot call cudaMalloc: plugins inside a framework that owns
+ * all device memory through its own caching allocator (a raw cudaMalloc
+ * would bypass its accounting), and serving loops that forbid allocation
+ * after start-up because cudaMalloc can synchronize the device and stall
+ * every stream.
  * This entry point takes the same arguments as bfq_gemm_block_fp8 minus the
  * workspace and computes the same result with the same launch plan.  No plan
  * needs scratch (K splits reduce through distributed shared memory), so it
@@ -342,7 +345,10 @@ bfq_status bfq_gemm_block_fp8_masked_silu_quant(const void* a_q, const void* a_s
 
 /*
  * Reads and clears the device-side error latch that kernel watchdogs set when
- * a bounded wait (on a TMA/MMA barrier) gives up.  Synchronizes `stream`.
+ * a bounded wait (on a TMA/MMA barrier) gives up.  The read and the clear are
+ * one atomic exchange on the device (a one-thread kernel on `stream`), so a
+ * timeout latched by a kernel on another stream is reported by this call or
+ * the next one, never lost.  Synchronizes `stream`.
  * Returns BFQ_OK, BFQ_ERR_TIMEOUT, or BFQ_ERR_CUDA.
  */
 bfq_status bfq_poll_device_status(void* stream);

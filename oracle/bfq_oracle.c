@@ -26,7 +26,7 @@
  *                 §4.2 (block-scaled GEMM: per-K-block dot times a_s * b_s),
  *                 §4.3 (metric formulas).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - e4m3 is the OCP "fn" variant (bias 7, max 448, no inf, S.1111.111 = NaN);
  *     conversion is round-to-nearest, ties to the even code, saturating to
  *     +-448 ("satfinite"); NaN converts to 0x7F.

@@ -56,6 +56,8 @@ def test_quant_validation(lib):
     assert q(None, 4, 256, 256, 128, 0, A16, A16, 4, None) == INVALID    # null x
     assert q(A16 + 2, 4, 256, 256, 128, 0, A16, A16, 4, None) == MISALIGNED
     assert q(A16, 4, 256, 260, 128, 0, A16, A16, 4, None) == MISALIGNED  # row stride
+    assert q(A16, 4, 256, 256, 128, 2, A16, A16, 6, None) == MISALIGNED  # scale_ld % 4
+    assert q(A16, 4, 256, 256, 128, 0, A16, A16, 5, None) == MISALIGNED
     assert q(A16, 0, 256, 256, 128, 0, None, None, 0, None) == OK        # empty: no-op
 
 
@@ -65,6 +67,7 @@ def test_silu_mul_quant_validation(lib):
     assert f(A16, 2, 16, 256, A16, 2, A16, A16, 8, None) == INVALID     # scale_ld < T
     assert f(A16, 2, 16, 256, None, 2, A16, A16, 16, None) == INVALID   # null counts
     assert f(A16 + 8, 2, 16, 256, A16, 2, A16, A16, 16, None) == MISALIGNED
+    assert f(A16, 2, 16, 256, A16, 2, A16, A16, 18, None) == MISALIGNED  # scale_ld % 4
     assert f(A16, 0, 16, 256, None, 2, None, None, 16, None) == OK      # no experts
 
 

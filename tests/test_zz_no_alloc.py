@@ -1,6 +1,6 @@
 """bfq_gemm_block_fp8_noalloc: the GEMM for callers that cannot allocate device
-memory (graph capture in global mode, frameworks that own all device memory,
-serving loops that forbid allocation after start-up).  No launch plan needs
+memory (plugins in frameworks that own all device memory, serving loops that
+forbid allocation after start-up).  No launch plan needs
 scratch (K splits reduce through distributed shared memory).
 
 The test calls it through the C ABI twice in a row, on shapes whose launch
