@@ -195,43 +195,93 @@ SAMPLE_COLS = 1024
 CPU_BASELINE_SECONDS = 10.0
 
 
-def oracle_sample_step(cols=SAMPLE_COLS):
-    """One bounded sample of the workload on the CPU oracle: 8 activation rows
-    against the first `cols` weight rows of each of the 6 (n, k) shapes (weight
-    block quant of that slice, activation quant, GEMM).  Returns FLOPs done."""
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_inputs(cols):
+    """Bounded sample inputs (bf16 bits): per (n, k), the first `cols` weight
+    rows and 8 activation rows."""
     import numpy as np
+    import torch
 
     import bfq_synth as synth
-    import oracle
 
-    flops = 0
+    out = []
     for n, k in SWEEP_NK:
         w = synth.weight(cols, k, seed=n + k)
         x = synth.activation(SAMPLE_ROWS, k, seed=SAMPLE_ROWS * 31 + n)
-        wb = w.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
-        xb = x.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
-        wq, sw = oracle.weight_block_quant(wb, False)
-        aq, sa = oracle.quant(xb, oracle.FMT_F32)
+        wb = w.contiguous().view(torch.int16).numpy().view(np.uint16)
+        xb = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+        out.append((k, wb, xb))
+    return out
+
+
+def oracle_sample_step(cols=SAMPLE_COLS, threads=1, inputs=None):
+    """One bounded sample of the workload on the CPU oracle: 8 activation rows
+    against the first `cols` weight rows of each of the 6 (n, k) shapes (weight
+    block quant of that slice, activation quant, GEMM).  With threads > 1 the
+    weight rows are shared out over that many host threads in 128-row blocks,
+    each thread quantizing its blocks and multiplying them (the oracle's C
+    code runs outside the interpreter lock; every block is computed exactly
+    as single-threaded).  Returns FLOPs done."""
+    import concurrent.futures as cf
+
+    import oracle
+
+    inputs = inputs or _oracle_inputs(cols)
+    flops = 0
+    acts = [oracle.quant(xb, oracle.FMT_F32) for _, _, xb in inputs]
+    blocks = [(i, c0) for i in range(len(inputs)) for c0 in range(0, cols, 128)]
+
+    def block(job):  # weight block quant + GEMM of one 128-row weight block
+        i, c0 = job
+        wq, sw = oracle.weight_block_quant(inputs[i][1][c0:c0 + 128], False)
+        aq, sa = acts[i]
         oracle.gemm(aq, sa, oracle.FMT_F32, wq, sw)
+
+    if threads <= 1:
+        for job in blocks:
+            block(job)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(block, blocks))
+    for k, _, _ in inputs:
         flops += 2 * SAMPLE_ROWS * cols * k
     return flops
 
 
+def _time_oracle(threads, seconds, cols=SAMPLE_COLS):
+    inputs = _oracle_inputs(cols)
+    t0 = time.perf_counter()
+    flops, reps = 0, 0
+    while reps == 0 or time.perf_counter() - t0 < seconds:
+        flops += oracle_sample_step(cols, threads, inputs)
+        reps += 1
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, reps, dt
+
+
 def cpu_baseline():
+    """The oracle timed on the host: on every host core (the reported value)
+    and on one thread, each for about CPU_BASELINE_SECONDS."""
     import oracle
 
     oracle.build_oracle()
-    # Repeat the bounded sample until about 10 s of CPU work has been timed.
-    t0 = time.perf_counter()
-    flops, reps = 0, 0
-    while reps == 0 or time.perf_counter() - t0 < CPU_BASELINE_SECONDS:
-        flops += oracle_sample_step()
-        reps += 1
-    dt = time.perf_counter() - t0
-    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{reps} x ({SAMPLE_ROWS} activation rows x first {SAMPLE_COLS} weight "
-                      f"rows of each of the 6 (n,k) sweep shapes: weight block quant + "
-                      f"activation quant + fp64 block GEMM), single thread ({dt:.1f} s)"}
+    oracle.e4m3_encode([0.0])  # build the oracle's tables before threads start
+    cores = host_cores()
+    v1, r1, d1 = _time_oracle(1, CPU_BASELINE_SECONDS)
+    vn, rn, dn = _time_oracle(cores, CPU_BASELINE_SECONDS)
+    what = (f"({SAMPLE_ROWS} activation rows x first {SAMPLE_COLS} weight rows of each of the "
+            f"6 (n,k) sweep shapes: weight block quant + activation quant + fp64 block GEMM)")
+    return {"value": vn, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{rn} x {what}, 128-row weight blocks shared over {cores} host threads "
+                      f"({dn:.1f} s)",
+            "single_thread": {"value": v1, "unit": UNIT, "cores": 1,
+                              "sample": f"{r1} x the same sample, one thread ({d1:.1f} s)"}}
 
 
 def run_reference(args, rank, world):
@@ -240,17 +290,20 @@ def run_reference(args, rank, world):
     import oracle
 
     oracle.build_oracle()
+    oracle.e4m3_encode([0.0])  # build the oracle's tables before threads start
+    cores = host_cores()
     # The weight-row sample shrinks with the number of steps so that the whole
-    # run stays near a minute and a half of CPU time (~2 s per step at 1024
-    # rows on the GPU machine's host cores).
+    # run stays near a minute and a half of CPU time (~2 s of single-thread
+    # work per step at 1024 rows on the GPU machine's host cores).
     cols = max(128, min(SAMPLE_COLS, SAMPLE_COLS * 40 // max(1, args.steps + args.warmup)
                         // 128 * 128))
+    inputs = _oracle_inputs(cols)
     for _ in range(args.warmup):
-        oracle_sample_step(cols)
+        oracle_sample_step(cols, cores, inputs)
     t0 = time.perf_counter()
     flops = 0
     for _ in range(args.steps):
-        flops += oracle_sample_step(cols)
+        flops += oracle_sample_step(cols, cores, inputs)
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
     line = {
@@ -258,9 +311,9 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "bounded CPU sample"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{SAMPLE_ROWS} rows x {cols} weight rows per (n,k), "
-                                   f"per step"},
+                                   f"per step, 128-row weight blocks over {cores} host threads"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -272,6 +325,11 @@ def run_reference(args, rank, world):
 # GPU arm
 # ---------------------------------------------------------------------------
 def build_problem(bfq, torch, dev, only=None):
+    """The 36 sweep shapes.  Every shape gets its own copy of its (n, k)
+    weight (quantized once, then cloned), so that no GEMM launch finds its
+    weights in L2: between two reads of one copy the step streams ~2.8 GB of
+    other weights (> 20x the 129 MB L2), as successive layers of a model do.
+    `wq0`/`sw0` keep the group's first copy for the L2-warm comparison."""
     import bfq_synth as synth
 
     shapes = []
@@ -279,19 +337,30 @@ def build_problem(bfq, torch, dev, only=None):
         if only and (only[1], only[2]) != (n, k):
             continue
         w = synth.weight(n, k, seed=n + k, device=dev)
-        wq, sw = bfq.weight_block_quant(w, bfq.SCALE_F32)
+        wq0, sw0 = bfq.weight_block_quant(w, bfq.SCALE_F32)
         del w
+        first = True
         for m in SWEEP_M:
             if only and only[0] != m:
                 continue
+            wq, sw = (wq0, sw0) if first else (wq0.clone(), sw0.clone())
+            first = False
             x = synth.activation(m, k, seed=m * 31 + n, device=dev)
             q = torch.empty((m, k), dtype=torch.float8_e4m3fn, device=dev)
             s = torch.empty((k // 128, bfq.align4(m)), dtype=torch.float32, device=dev)
             out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
             ws = bfq.gemm_workspace(m, n, k, dev)
-            shapes.append(dict(m=m, n=n, k=k, x=x, q=q, s=s, wq=wq, sw=sw, out=out, ws=ws))
+            shapes.append(dict(m=m, n=n, k=k, x=x, q=q, s=s, wq=wq, sw=sw, wq0=wq0, sw0=sw0,
+                               out=out, ws=ws))
     torch.cuda.synchronize()
     return shapes
+
+
+def warm_view(shapes):
+    """The same shapes with every (n, k) group sharing one weight copy: the
+    m = 64 .. 4096 launches then find weights the previous launch of the
+    group left in L2 (the pages' benchmark loop repeats one weight)."""
+    return [dict(sh, wq=sh["wq0"], sw=sh["sw0"]) for sh in shapes]
 
 
 def step(bfq, shapes, events=None):
@@ -402,6 +471,124 @@ def timed_launches(bfq, torch, shapes, reps):
             qt[j].append(ev[j][0].elapsed_time(ev[j][1]))
             gt[j].append(ev[j][1].elapsed_time(ev[j][2]))
     return qt, gt
+
+
+def measure_calc_diff(bfq, torch, dev, shapes, threads):
+    """Per shape, on sampled rows (first, last and two seeded rows): the pages'
+    calc_diff ("vLLM DeepGEMM FP8 Block GEMM 基准测试" §4.4: 1 - 2<x,y> /
+    (|x|^2 + |y|^2), in fp64) between the GPU's bf16 output and the oracle's
+    fp64 result, and the largest error normalised by |A_hat[m]| |W_hat[n]|
+    (the 2e-3 gate of the parity tests).  The oracle quantizes the same
+    seeded bf16 inputs itself; its weight quant and GEMM are shared out over
+    `threads` host threads in 128-row weight blocks."""
+    import concurrent.futures as cf
+
+    import numpy as np
+
+    import bfq_synth as synth
+    import oracle
+
+    oracle.build_oracle()
+    oracle.e4m3_encode([0.0])  # build the oracle's tables before threads start
+    res = []
+    groups = {}
+    for sh in shapes:
+        groups.setdefault((sh["n"], sh["k"]), []).append(sh)
+    with cf.ThreadPoolExecutor(max_workers=max(1, threads)) as ex:
+        for (n, k), grp in groups.items():
+            w = synth.weight(n, k, seed=n + k, device=dev)
+            wb = w.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+            del w
+            blocks = list(range(0, n, 128))
+            parts = list(ex.map(lambda r0: oracle.weight_block_quant(wb[r0:r0 + 128], False),
+                                blocks))
+            wq = np.concatenate([p_[0] for p_ in parts])
+            sw = np.concatenate([p_[1] for p_ in parts])
+            wn = np.concatenate(list(ex.map(
+                lambda p_: np.linalg.norm(oracle.dequant_weight(p_[0], p_[1]), axis=1), parts)))
+            for sh in grp:
+                m = sh["m"]
+                rng = np.random.default_rng(m * 7 + n + k)
+                rows = np.unique(np.concatenate([[0, m - 1], rng.integers(0, m, 2)]))
+                xb = sh["x"][torch.from_numpy(rows).to(dev)].cpu().contiguous()
+                aq, sa = oracle.quant(xb.view(torch.int16).numpy().view(np.uint16),
+                                      oracle.FMT_F32)
+                ref = np.concatenate(list(ex.map(
+                    lambda i: oracle.gemm(aq, sa, oracle.FMT_F32, parts[i][0], parts[i][1]),
+                    range(len(parts)))), axis=1)
+                got = sh["out"][torch.from_numpy(rows).to(dev)].float().cpu().numpy()
+                an = np.linalg.norm(oracle.dequant_rows(aq, sa, oracle.FMT_F32), axis=1)
+                x64, y64 = got.astype(np.float64), ref
+                den = (x64 * x64 + y64 * y64).sum()
+                cd = float(1.0 - 2.0 * (x64 * y64).sum() / den) if den > 0 else 0.0
+                err = np.abs(x64 - y64) / (an[:, None] * wn[None, :])
+                res.append({"m": m, "n": n, "k": k, "rows": len(rows), "calc_diff": cd,
+                            "max_norm_err": float(err.max())})
+            del wb, wq, sw, parts
+    return res
+
+
+def measure_pdl_ab(bfq, torch, shapes, replays):
+    """Programmatic dependent launch on and off ("vLLM DeepGEMM FP8 Block GEMM
+    基准测试" §4.2: the wrapper enables PDL).  (1) The decode chain of the
+    smallest dense case, quant 8 x 7168 -> GEMM 8 x 4096 x 7168, back to back
+    in one graph over nine weight copies (> 2x L2, so every GEMM reads its
+    weights from HBM); (2) the whole sweep step as one graph.  Each graph is
+    captured with the switch set, so it holds that launch mode."""
+    c0 = next((sh for sh in shapes if (sh["m"], sh["n"], sh["k"]) == (8, 4096, 7168)), None)
+    res = {}
+    if c0 is not None:
+        copies = 9
+        wqs = [c0["wq"]] + [c0["wq"].clone() for _ in range(copies - 1)]
+        sws = [c0["sw"]] + [c0["sw"].clone() for _ in range(copies - 1)]
+        ld = c0["s"].shape[-1]
+
+        def chain(i):
+            bfq.bfq_quant(c0["x"], c0["q"], c0["s"], bfq.SCALE_F32, ld)
+            bfq.bfq_gemm_block_fp8(c0["q"], c0["s"], bfq.SCALE_F32, ld, wqs[i], sws[i],
+                                   c0["out"], c0["ws"])
+
+        def gemm_only(i):
+            bfq.bfq_gemm_block_fp8(c0["q"], c0["s"], bfq.SCALE_F32, ld, wqs[i], sws[i],
+                                   c0["out"], c0["ws"])
+
+        for name, fn in (("c0_quant_gemm_chain_us", chain), ("c0_gemm_us", gemm_only)):
+            res[name] = {}
+            for mode in (True, False):
+                prev = bfq.bfq_set_programmatic_launch(mode)
+                try:
+                    t = graph_back_to_back_us(torch, fn, copies, 4 * copies)
+                finally:
+                    bfq.bfq_set_programmatic_launch(prev)
+                res[name]["pdl" if mode else "no_pdl"] = round(t, 2)
+        del wqs, sws
+    res["step_ms"] = {}
+    for mode in (True, False):
+        prev = bfq.bfq_set_programmatic_launch(mode)
+        try:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                step(bfq, shapes)
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g, stream=side):
+                    step(bfq, shapes)
+            torch.cuda.current_stream().wait_stream(side)
+        finally:
+            bfq.bfq_set_programmatic_launch(prev)
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(replays):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        res["step_ms"]["pdl" if mode else "no_pdl"] = round(e0.elapsed_time(e1) / replays, 4)
+        del g
+    return res
 
 
 QUANT_M = [8, 128, 4096, 16384]
@@ -706,6 +893,8 @@ def run_gpu(args, rank, world, local_rank):
 
     reps = max(3, min(args.steps, 20))
     qts, gts = timed_launches(bfq, torch, shapes, reps)
+    parity = measure_calc_diff(bfq, torch, dev, shapes, host_cores()) if rank == 0 else []
+    _, gts_warm = timed_launches(bfq, torch, warm_view(shapes), reps)
     status = bfq.bfq_poll_device_status()
     if status != 0:
         raise RuntimeError(f"device watchdog reported status {status}")
@@ -731,7 +920,12 @@ def run_gpu(args, rank, world, local_rank):
             "bound": "tensor" if t_flop >= t_byte else "hbm",
             "quant_us": round(q_us, 2),
             "quant_gbps": round(quant_alg_bytes(m, k) / (q_us * 1e-6) / 1e9, 1),
+            "gemm_us_l2warm": round(statistics.median(gts_warm[j]) * 1e3, 2),
         })
+        pr = next((r for r in parity if (r["m"], r["n"], r["k"]) == (m, n, k)), None)
+        if pr:
+            per_shape[-1]["calc_diff"] = float(f"{pr['calc_diff']:.3e}")
+            per_shape[-1]["max_norm_err"] = float(f"{pr['max_norm_err']:.3e}")
     gemm_launch_ms = gemm_ms_total / (reps * n_shapes)
     achieved_tflops = flops_step * reps / (gemm_ms_total * 1e-3) / 1e12
     gemm_bytes_avg = sum(gemm_alg_bytes(s["m"], s["n"], s["k"]) for s in shapes) / n_shapes
@@ -774,8 +968,10 @@ def run_gpu(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD, "shapes": n_shapes, "act_scales": "fp32 col-major",
                    "weight_scales": "fp32 128x128", "parallelism": f"replicas x{world}",
                    "timed": "CUDA graph of the whole step (quant + GEMM per shape), replayed",
-                   "l2": "no flush: one step streams ~1.2 GB of distinct operands (> 129 MB "
-                         "L2) before any shape repeats"},
+                   "l2": "inputs larger than L2: every shape reads its own weight copy "
+                         "(~2.8 GB of distinct weights per step, > 20x the 129 MB L2), so no "
+                         "GEMM launch finds its weights in L2; per-shape gemm_us_l2warm "
+                         "re-times the step with one weight copy per (n,k) group"},
         "e2e": {"value": world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.steps,
@@ -800,8 +996,16 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk.summary(),
         "shapes": per_shape,
     }
+    if parity:
+        line["parity"] = {
+            "vs": "CPU oracle (fp64 block GEMM of its own quantization of the same inputs)",
+            "rows_per_shape": "first, last and two seeded rows, every column",
+            "calc_diff_max": float(f"{max(r['calc_diff'] for r in parity):.3e}"),
+            "max_norm_err": float(f"{max(r['max_norm_err'] for r in parity):.3e}"),
+            "gate": 2e-3}
     if not args.skip_extra:
-        del shapes
+        line["pdl_ab"] = measure_pdl_ab(bfq, torch, shapes, 10)
+        del shapes, pipe
         torch.cuda.empty_cache()
         line["quant_sweep"] = measure_quant_sweep(bfq, torch, dev, hbm_peak, 10)
         line["moe_slice"] = measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, 10)

@@ -78,6 +78,7 @@ def load_library(build: bool = True):
                                                           I64, I32, P, P, I64, P]),
             "bfq_gemm_noalloc_scratch_bytes": (SZ, []),
             "bfq_poll_device_status": (I32, [P]),
+            "bfq_set_programmatic_launch": (I32, [I32]),
             "bfq_watchdog_selftest": (I32, [I32, P]),
         }
         for name, (res, args) in sig.items():
@@ -268,6 +269,12 @@ def bfq_gemm_block_fp8_masked(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w
 
 def bfq_poll_device_status(stream=None) -> int:
     return int(load_library().bfq_poll_device_status(_stream(stream)))
+
+
+def bfq_set_programmatic_launch(enable: bool) -> bool:
+    """Switch programmatic dependent launch for later launches; returns the
+    previous setting."""
+    return bool(load_library().bfq_set_programmatic_launch(1 if enable else 0))
 
 
 def bfq_watchdog_selftest(timeout_us: int, stream=None) -> None:

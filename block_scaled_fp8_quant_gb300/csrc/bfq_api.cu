@@ -1,5 +1,6 @@
 // bfq_api.cu — host-side plumbing of the C ABI: version, status strings,
 // per-device facts, the device error latch and the watchdog self-test.
+#include <atomic>
 #include <mutex>
 
 #include "bfq_device.cuh"
@@ -11,11 +12,14 @@ __device__ int g_device_status = 0;
 __device__ int g_status_taken = 0;
 
 namespace {
+std::atomic<int> g_pdl{1};
 constexpr int kMaxDevices = 64;
 DeviceInfo g_info[kMaxDevices];
 int* g_status_ptr[kMaxDevices];
 std::mutex g_info_mu;
 }  // namespace
+
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 
 int* device_status_ptr() {
   int dev = -1;
@@ -107,6 +111,10 @@ extern "C" const char* bfq_status_string(bfq_status status) {
     case BFQ_ERR_DEVICE: return "BFQ_ERR_DEVICE";
     default: return "BFQ_ERR_UNKNOWN";
   }
+}
+
+extern "C" int32_t bfq_set_programmatic_launch(int32_t enable) {
+  return g_pdl.exchange(enable ? 1 : 0);
 }
 
 extern "C" bfq_status bfq_poll_device_status(void* stream) {

@@ -40,10 +40,15 @@ inline bfq_status launch_status(cudaError_t e) {
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Whether launches use programmatic stream serialization (process-wide,
+// default on; bfq_set_programmatic_launch switches it for measurements).
+bool pdl_enabled();
+
 // Launch `kernel` on `stream` with programmatic stream serialization (the
 // kernel may start before the previous one in the stream has finished; it
 // waits in griddep_wait() before touching memory) and an optional cluster
-// size along x.
+// size along x.  With programmatic launch switched off the kernel is
+// launched with plain stream order (griddep_wait() is then a no-op).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, unsigned cluster_x, Args&&... args) {
@@ -54,9 +59,11 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   unsigned n = 0;
-  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[n].val.programmaticStreamSerializationAllowed = 1;
-  ++n;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   if (cluster_x > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = cluster_x;

@@ -344,6 +344,19 @@ bfq_status bfq_gemm_block_fp8_masked_silu_quant(const void* a_q, const void* a_s
                                                 void* stream);
 
 /*
+ * Process-wide switch for programmatic dependent launch ([DG-bench] §4.2: the
+ * GEMM wrapper enables PDL so that a kernel's set-up overlaps the tail of the
+ * kernel before it).  enable != 0 (the default): every kernel is launched
+ * with programmatic stream serialization, as described in the conventions
+ * above.  enable == 0: plain stream order, each kernel scheduled only after
+ * the previous one has finished.  Results are bit-identical either way; the
+ * switch exists to measure what the overlap buys.  It applies to launches
+ * made (or captured into a graph) after the call.  Returns the previous
+ * setting (0 or 1).
+ */
+int32_t bfq_set_programmatic_launch(int32_t enable);
+
+/*
  * Reads and clears the device-side error latch that kernel watchdogs set when
  * a bounded wait (on a TMA/MMA barrier) gives up.  The read and the clear are
  * one atomic exchange on the device (a one-thread kernel on `stream`), so a

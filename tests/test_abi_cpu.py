@@ -110,3 +110,11 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
         pytest.skip("this machine has a GPU")
     assert lib.bfq_quant(A16, 4, 256, 256, 128, 0, A16, A16, 4, None) == CUDA
     assert lib.bfq_gemm_workspace_bytes(8, 4096, 7168) == 0
+
+
+def test_programmatic_launch_switch(lib):
+    """The process-wide PDL switch returns the previous setting (default on)."""
+    assert lib.bfq_set_programmatic_launch(0) == 1
+    assert lib.bfq_set_programmatic_launch(0) == 0
+    assert lib.bfq_set_programmatic_launch(5) == 0   # any non-zero value means on
+    assert lib.bfq_set_programmatic_launch(1) == 1
