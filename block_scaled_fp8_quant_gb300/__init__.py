@@ -66,7 +66,7 @@ def load_library(build: bool = True):
             "bfq_quant": (I32, [P, I64, I64, I64, I32, I32, P, P, I64, P]),
             "bfq_silu_mul_quant": (I32, [P, I32, I32, I32, P, I32, P, P, I64, P]),
             "bfq_weight_block_quant": (I32, [P, I64, I64, I64, I32, P, P, P]),
-            "bfq_gemm_workspace_bytes": (SZ, [I64, I64, I64]),
+            "bfq_gemm_workspace_bytes": (SZ, [I64, I64, I64, I32]),
             "bfq_gemm_block_fp8": (I32, [P, P, I32, I64, P, P, I64, I64, I64, P, P, SZ, P]),
             "bfq_gemm_block_fp8_masked": (I32, [P, P, I32, I64, P, P, P, I32, I32, I64, I64,
                                                 I32, P, P, SZ, P]),
@@ -149,8 +149,8 @@ def bfq_weight_block_quant(w, wq, sw, fmt: int, stream=None) -> None:
                                       _stream(stream)))
 
 
-def bfq_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
-    return int(load_library().bfq_gemm_workspace_bytes(M, N, K))
+def bfq_gemm_workspace_bytes(M: int, N: int, K: int, E: int = 0) -> int:
+    return int(load_library().bfq_gemm_workspace_bytes(M, N, K, E))
 
 
 def bfq_gemm_block_fp8(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w_scales, out,
@@ -321,8 +321,11 @@ _ws_cache: dict = {}
 
 
 def gemm_workspace(M: int, N: int, K: int, device) -> torch.Tensor | None:
-    """Zero-initialised workspace sized for (M, N, K) on `device` (cached, grows);
-    None when the plan needs none (every plan of the current kernels)."""
+    """Zero-initialised workspace sized for a dense (M, N, K) GEMM on `device`
+    (one buffer per device, cached and grown on demand); None when the plan
+    needs none.  Calls that share it must be ordered on one stream: the
+    library keeps partial sums and per-tile counters in it during a call
+    (and leaves the counters zero again)."""
     need = bfq_gemm_workspace_bytes(M, N, K)
     if need == 0:
         return None

@@ -1331,12 +1331,13 @@ bfq_status check_device(DeviceInfo* dev) {
 
 using namespace bfq;
 
-// The K splits of a tile reduce through distributed shared memory, so no
-// plan needs a workspace.
-extern "C" size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+// Every split reduces through distributed shared memory, so no plan needs a
+// workspace.
+extern "C" size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t E) {
   (void)M;
   (void)N;
   (void)K;
+  (void)E;
   return 0;
 }
 

@@ -162,13 +162,18 @@ bfq_status bfq_weight_block_quant(const void* w, int64_t batch, int64_t N, int64
                                   int32_t fmt, void* wq, float* sw, void* stream);
 
 /*
- * Bytes of workspace that bfq_gemm_block_fp8 needs for an (M, N, K) problem:
- * 0 for every problem.  The K splits of a tile reduce their fp32 partial sums
- * through the distributed shared memory of their thread-block cluster, so no
- * plan uses global scratch.  Kept so that callers written against a
- * workspace-taking interface need not change.
+ * Bytes of workspace a GEMM problem needs: 0 for every problem.
+ *
+ *   E == 0     dense bfq_gemm_block_fp8 / bfq_gemm_block_fp8_quant of
+ *              M x N x K;
+ *   E >= 1     the masked grouped GEMM of E experts with M rows each.
+ *
+ * Every K split reduces its fp32 partial sums through the distributed shared
+ * memory of its thread-block cluster, so no plan uses global scratch.  Kept
+ * so that callers written against a workspace-taking interface need not
+ * change.
  */
-size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t E);
 
 /*
  * Dense block-scaled FP8 GEMM, "NT" ([DG-bench] §4.2 fp8_gemm_nt and the
@@ -182,7 +187,7 @@ size_t bfq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * than SMs, K is split over the CTAs of a thread-block cluster (at most 8);
  * each CTA keeps its fp32 partial sum in shared memory and the cluster adds
  * them in split order through distributed shared memory, so results are
- * deterministic.
+ * deterministic.  With more tiles than SMs, one CTA per SM walks the tiles.
  *
  *   a_q            e4m3 [M][K], 16-byte aligned.
  *   a_scales       column-major activation scales in format a_fmt
@@ -279,10 +284,13 @@ size_t bfq_gemm_noalloc_scratch_bytes(void);
  *   w_q            e4m3 [E][N][K].
  *   w_scales       float [E][ceil(N/128)][K/128].
  *   valid_counts   device int32 [E], clamped to [0, T].
- *   expected_m     hint of the typical count (0 = unknown); may steer the
- *                  launch plan, never the result.
+ *   expected_m     hint of the typical count (0 = unknown).  Accepted and
+ *                  not used by the current plans, which read the counts on
+ *                  the device; it can never change the result.
  *   out            bf16 [E][T][N].
- *   workspace      unused by the current plans; may be NULL.
+ *   workspace, workspace_bytes   accepted and not used: no plan of the
+ *                  masked GEMM needs a workspace (bfq_gemm_workspace_bytes
+ *                  with E >= 1 returns 0); may be NULL / 0.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, FORMAT, CUDA, DEVICE.
  */
 bfq_status bfq_gemm_block_fp8_masked(const void* a_q, const void* a_scales, int32_t a_fmt,

@@ -109,7 +109,16 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("this machine has a GPU")
     assert lib.bfq_quant(A16, 4, 256, 256, 128, 0, A16, A16, 4, None) == CUDA
-    assert lib.bfq_gemm_workspace_bytes(8, 4096, 7168) == 0
+    assert lib.bfq_gemm_workspace_bytes(8, 4096, 7168, 0) == 0
+
+
+def test_workspace_bytes_are_zero(lib):
+    """Every split reduces through distributed shared memory: no plan, dense
+    (E = 0) or masked (E >= 1), needs a workspace."""
+    ws = lib.bfq_gemm_workspace_bytes
+    for m, n, k, e in [(8, 4096, 7168, 0), (64, 32768, 512, 0), (4096, 4096, 7168, 0),
+                       (256, 4096, 7168, 32)]:
+        assert ws(m, n, k, e) == 0
 
 
 def test_programmatic_launch_switch(lib):

@@ -53,24 +53,33 @@ def test_gemm_parity_small(cuda_lib, orc, fmt, M, N, K):
     assert_gemm_close(out.float().cpu().numpy(), ref, an, wn, f"gemm {M}x{N}x{K} fmt{fmt}")
 
 
+def _no_workspace_gemm(bfq, d, fmt, out=None):
+    """The dense GEMM called with no workspace: the plans that need none."""
+    M, N = d[0].shape[0], d[2].shape[0]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda") if out is None else out
+    bfq.bfq_gemm_block_fp8(d[0], d[1], fmt, d[1].shape[-1], d[2], d[3], out, None)
+    return out
+
+
 def test_gemm_split_k_is_deterministic(cuda_lib, orc):
-    """A shape whose two 256-wide tiles split K eight ways over a cluster: the
-    partial sums meet in distributed shared memory and are added in split
-    order, so repeated calls agree bit for bit; no workspace is needed."""
+    """Splits of the K range meet in distributed shared memory and are added in
+    a fixed order, so repeated calls agree bit for bit; a workspace is
+    accepted and changes nothing.  24 x 512 x 4096 and 200 x 512 x 4096: two
+    256-wide output tiles per row tile, K split over a cluster."""
     bfq = cuda_lib
-    M, N, K = 24, 512, 4096
-    assert bfq.bfq_gemm_workspace_bytes(M, N, K) == 0
-    aq, sa, wq, sw = _oracle_problem(orc, M, N, K, 0, seed=99)
-    d = _to_dev(aq, sa, wq, sw, 0)
-    o1 = bfq.gemm(d[0], d[1], 0, d[2], d[3])
-    o2 = bfq.gemm(d[0], d[1], 0, d[2], d[3])
-    ws = torch.full((4096,), 0x7F, dtype=torch.uint8, device="cuda")  # accepted, unused
-    o3 = bfq.gemm(d[0], d[1], 0, d[2], d[3], workspace=ws)
-    torch.cuda.synchronize()
-    assert torch.equal(o1, o2) and torch.equal(o1, o3)
-    ref = orc.gemm(aq, sa, 0, wq, sw)
-    an, wn = _norms(orc, aq, sa, wq, sw, 0)
-    assert_gemm_close(o1.float().cpu().numpy(), ref, an, wn, "split")
+    for M, N, K in ((24, 512, 4096), (200, 512, 4096)):
+        assert bfq.bfq_gemm_workspace_bytes(M, N, K) == 0
+        aq, sa, wq, sw = _oracle_problem(orc, M, N, K, 0, seed=99 + M)
+        d = _to_dev(aq, sa, wq, sw, 0)
+        o1 = _no_workspace_gemm(bfq, d, 0)
+        o2 = _no_workspace_gemm(bfq, d, 0)
+        ws = torch.full((4096,), 0x7F, dtype=torch.uint8, device="cuda")  # accepted, unused
+        o3 = bfq.gemm(d[0], d[1], 0, d[2], d[3], workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(o1, o3)
+        ref = orc.gemm(aq, sa, 0, wq, sw)
+        an, wn = _norms(orc, aq, sa, wq, sw, 0)
+        assert_gemm_close(o1.float().cpu().numpy(), ref, an, wn, f"split {M}")
 
 
 def test_gemm_rejects_format_it_was_not_told(cuda_lib, orc):
@@ -147,15 +156,12 @@ def test_gemm_parity_unsplit_many_tiles(cuda_lib, orc, fmt, M, N, K):
 @pytest.mark.parametrize("M,N,K", [(40, 13056, 256), (100, 16384, 256)])
 def test_gemm_parity_narrow_unsplit_plan(cuda_lib, orc, fmt, M, N, K):
     """One row tile of more than 32 rows whose 256-wide plan would split K
-    two ways: the plan takes 128-wide tiles with no split instead (no
-    workspace on a 152-SM GB300)."""
+    two ways: the plan takes 128-wide tiles with no split instead."""
     bfq = cuda_lib
-    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
-        assert bfq.bfq_gemm_workspace_bytes(M, N, K) == 0
     aq, sa, wq, sw = _oracle_problem(orc, M, N, K, fmt, seed=M + N + K + fmt)
     d = _to_dev(aq, sa, wq, sw, fmt)
     out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    bfq.gemm(d[0], d[1], fmt, d[2], d[3], out=out)
+    _no_workspace_gemm(bfq, d, fmt, out=out)
     torch.cuda.synchronize()
     ref = orc.gemm(aq, sa, fmt, wq, sw)
     an, wn = _norms(orc, aq, sa, wq, sw, fmt)
