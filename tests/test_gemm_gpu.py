@@ -83,18 +83,31 @@ def test_gemm_split_k_is_deterministic(cuda_lib, orc):
 
 
 def test_gemm_rejects_format_it_was_not_told(cuda_lib, orc):
-    """Packed exponents passed as fp32 scales give wrong results; passing the
-    right format gives the right ones (the scale-format mismatch reported in
-    the review of "[Perf] Deepgemm fused layout kernel for activations")."""
+    """The scale format travels with the scales: UE8M0 words handed to the GEMM
+    as packed give the oracle's result, while the same words handed over as
+    fp32 scales give a result far outside the tolerance (the mismatch
+    reported in the review of "[Perf] Deepgemm fused layout kernel for
+    activations", where packed exponents were read as floats).  The fp32 call
+    gets a buffer sized for fp32 scales (the packed words in its first
+    columns, zeros after) so that every read stays inside it."""
     bfq = cuda_lib
     M, N, K = 16, 256, 1024
     aq, sa, wq, sw = _oracle_problem(orc, M, N, K, 2, seed=5)
     d = _to_dev(aq, sa, wq, sw, 2)
     good = bfq.gemm(d[0], d[1], 2, d[2], d[3])
+    ld = d[1].shape[-1]
+    as_f32 = torch.zeros((K // 128, ld), dtype=torch.int32, device="cuda")
+    as_f32[:K // 512] = d[1]
+    bad = bfq.gemm(d[0], as_f32.view(torch.float32), 0, d[2], d[3])
     torch.cuda.synchronize()
     ref = orc.gemm(aq, sa, 2, wq, sw)
     an, wn = _norms(orc, aq, sa, wq, sw, 2)
     assert_gemm_close(good.float().cpu().numpy(), ref, an, wn, "packed")
+    got = bad.float().cpu().numpy()
+    with np.errstate(invalid="ignore", over="ignore"):
+        err = np.abs(got.astype(np.float64) - ref) / (an[:, None] * wn[None, :])
+    assert not (np.isfinite(got).all() and err.max() <= 2e-3), \
+        "packed words read as fp32 scales must not pass the tolerance"
 
 
 SWEEP_NK = [(4096, 7168), (7168, 18432), (18432, 7168), (24576, 1536), (32768, 512),

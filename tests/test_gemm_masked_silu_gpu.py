@@ -78,14 +78,25 @@ def test_fused_silu_quant_equals_unfused_chain(cuda_lib, orc, fmt, E, T, H, I, c
 
 
 @pytest.mark.slow
-def test_fused_silu_quant_moe_config(cuda_lib):
+def test_fused_silu_quant_moe_config(cuda_lib, orc):
     """The MoE config (E=32, T=256, H=7168, I=2048, counts ~U{0..256}, packed
-    UE8M0): fused equals the unfused chain on every valid row."""
+    UE8M0): fused equals the unfused chain on every valid row, and on sampled
+    rows (the first and last four valid rows of three experts) the fused
+    codes and scales match the oracle's own chain — its quant of the same
+    activations, fp64 up projection rounded to bf16, silu-mul-quant — up to
+    the rare code that an ulp of the bf16 up output can move."""
     bfq = cuda_lib
     E, T, H, I = 32, 256, 7168, 2048
     counts = synth.valid_counts(E, T)
     d_cnt = counts.cuda()
     x = synth.masked_activation(E, T, H, counts, seed=900, device="cuda", poison=False)
+    live = [e for e in range(E) if int(counts[e]) > 0]
+    sample = sorted({live[0], live[len(live) // 2], live[-1]})
+    x_rows = {}
+    for e in sample:
+        c = int(counts[e])
+        rows = sorted({0, 1, 2, 3, c - 4, c - 3, c - 2, c - 1} & set(range(c)))
+        x_rows[e] = (rows, bits(x[e, torch.tensor(rows, device="cuda")]))
     a = torch.zeros((E, T, H), dtype=torch.float8_e4m3fn, device="cuda")
     sa = torch.zeros((E, bfq.scale_cols(H, 2), T), dtype=torch.int32, device="cuda")
     for e in range(E):
@@ -110,3 +121,27 @@ def test_fused_silu_quant_moe_config(cuda_lib):
         c = int(counts[e])
         assert np.array_equal(qf[e, :c], qu[e, :c]), f"expert {e}"
         assert np.array_equal(sf[e][:, :c], su[e][:, :c]), f"expert {e}"
+    # the oracle's chain on the sampled rows
+    dec = orc.e4m3_decode_table()
+    for e in sample:
+        rows, xb = x_rows[e]
+        n = len(rows)
+        owq, osw = orc.weight_block_quant(bits(synth.weight(2 * I, H, seed=700 + e,
+                                                           device="cuda")), True)
+        oq, osa = orc.quant(xb, 2)
+        up = orc.gemm(oq, osa, 2, owq, osw)                      # fp64 [n, 2I]
+        hb = bits(torch.from_numpy(up).to(torch.bfloat16))       # bf16 RNE, as stored
+        yq, ys = orc.silu_mul_quant(hb.reshape(1, n, 2 * I), np.array([n], np.int32), 2)
+        got_q, got_s = qf[e, rows], sf[e][:, rows]
+        ref_q, ref_s = yq[0], ys[0][:, :n]
+        assert (got_s == ref_s).mean() >= 0.99, f"expert {e}: scales"
+        # codes of the groups whose packed scale word agrees (a group's scale
+        # moves only if an ulp of its amax crosses a power of two)
+        words_ok = (got_s == ref_s).T                                   # [n, I/512]
+        group_ok = np.repeat(words_ok, 512, axis=1)[:, :I]              # [n, I]
+        same = (got_q == ref_q) | ~group_ok
+        assert same.mean() >= 0.999, f"expert {e}: {int((~same).sum())} codes differ"
+        # a differing code is at most one e4m3 step away
+        diff = np.abs(dec[got_q[~same]] - dec[ref_q[~same]])
+        step = np.maximum(np.abs(dec[ref_q[~same]]) * 2.0 ** -3, 2.0 ** -9)
+        assert (diff <= step * 1.0001).all(), f"expert {e}: a code moved by more than one step"
