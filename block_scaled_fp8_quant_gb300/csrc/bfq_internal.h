@@ -76,6 +76,13 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// silu(g) of every bf16 gate g (indexed by its 16 bits), evaluated once per
+// device by the library's fp32 silu; built on the first call that is not
+// being captured into a CUDA graph (the build synchronizes `stream` once).
+// Null while `stream` is capturing and the table is not built yet.  Defined
+// in quant_kernels.cu.
+const float* silu_table(const DeviceInfo& dev, cudaStream_t stream);
+
 // Columns of a column-major scale array for K elements per row.
 inline int64_t scale_cols(int64_t K, int32_t fmt) {
   return fmt == BFQ_SCALE_UE8M0_PACKED ? cdiv(K / 128, 4) : K / 128;

@@ -92,6 +92,9 @@ struct GemmParams {
   void* q_scales;
   int64_t q_scale_ld;
   int q_fmt;
+  // fused silu-mul-quant (SILU kernel): silu of every bf16 gate, indexed by
+  // its 16 bits (the library's table), or null to compute it
+  const float* silu_tab;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -950,7 +953,9 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
       if constexpr (SILU) {
         // Fused silu(gate) * up + 1 x 128 group quant of the features of this
         // tile, exactly as the silu-mul-quant kernel computes them from the
-        // bf16 up-projection output ("[EP+DP] Optimize the little operations
+        // bf16 up-projection output (silu looked up in the library's table of
+        // all bf16 gates, or computed while a graph is captured before the
+        // table exists — the same values) ("[EP+DP] Optimize the little operations
         // in the DeepGEMM + DeepEP low latency case", Summary item 2): gate
         // and up rounded to bf16, y = silu(g) * u in fp32, group amax over the
         // 128 features (this thread's 64 and the other half-warp's 64,
@@ -961,7 +966,10 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
           for (int j = 0; j < 32; ++j) {
             const float2 gf = unpack2(acc[j]), uf = unpack2(acc[32 + j]);
             const uint32_t gb = pack_bf16x2(gf.x, gf.y), ub = pack_bf16x2(uf.x, uf.y);
-            const float2 sg = bfq_silu2(bf16lo(gb), bf16hi(gb));
+            const float2 sg = p.silu_tab
+                                  ? make_float2(__ldg(p.silu_tab + (gb & 0xFFFFu)),
+                                                __ldg(p.silu_tab + (gb >> 16)))
+                                  : bfq_silu2(bf16lo(gb), bf16hi(gb));
             const float2 y = unpack2(mul2_rn(pack2(sg.x, sg.y), pack2(bf16lo(ub), bf16hi(ub))));
             acc[j] = pack2(y.x, y.y);
             amax = fmaxf(amax, fmaxf(fabsf(y.x), fabsf(y.y)));
@@ -1618,6 +1626,7 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked_silu_quant(
   p.q_scales = q_scales;
   p.q_scale_ld = q_scale_ld;
   p.q_fmt = q_fmt;
+  p.silu_tab = silu_table(dev, (cudaStream_t)stream);
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles * E;
   const unsigned grid = (unsigned)(tiles < dev.sm_count ? tiles : dev.sm_count);
   return launch_persistent<true, false, true>(dev, ma, mw, mw, p, grid, (cudaStream_t)stream);

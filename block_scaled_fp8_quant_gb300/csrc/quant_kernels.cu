@@ -15,6 +15,8 @@
 // owns elements [16 l, 16 l + 16) and group l / 8; the 8 lanes of a group
 // reduce their amax with three xor-shuffles.  Loads are 16-byte, coalesced
 // (a warp reads 1 KiB of bf16 contiguous memory per unit) and bypass L1.
+#include <mutex>
+
 #include "bfq_device.cuh"
 
 namespace bfq {
@@ -146,17 +148,30 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 // ---------------------------------------------------------------------------
 // fused silu-and-mul + quant over a masked per-expert batch
 // ---------------------------------------------------------------------------
-// Two rows per block and one unit in flight per warp: the kernel is bound by
-// the exp and division of silu, and small blocks keep more warps resident
-// (fewer registers each) and spread the valid rows evenly over the SMs.
+// The gate is a bf16 value, so silu takes one of 65536 inputs: the library
+// evaluates bfq_silu for every one of them once per device into this table
+// (indexed by the gate's 16 bits), and the kernel looks silu up instead of
+// spending ~40 instructions per element on the exp polynomial and the IEEE
+// division.  The values are those of bfq_silu bit for bit.
+__device__ float g_silu_table[65536];
+
+__global__ void __launch_bounds__(256) silu_table_kernel(float* __restrict__ table) {
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  table[i] = bfq_silu(__uint_as_float((uint32_t)i << 16));
+}
+
+// Two rows per block and one unit in flight per warp: small blocks keep more
+// warps resident and spread the valid rows evenly over the SMs.  TABLE:
+// silu by table lookup; otherwise computed (the same values).
 constexpr int kSiluRowsPerBlock = 2;
 constexpr int kSiluUnroll = 1;
 
-template <int FMT>
+template <int FMT, bool TABLE>
 __global__ void __launch_bounds__(kQuantWarps * 32)
     silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int I,
                           const int32_t* __restrict__ counts, uint8_t* __restrict__ q,
-                          void* __restrict__ scales, int64_t scale_ld) {
+                          void* __restrict__ scales, int64_t scale_ld,
+                          const float* __restrict__ silu_tab) {
   griddep_wait();
   griddep_launch_dependents();
   const int e = blockIdx.y;
@@ -203,9 +218,17 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       float g[16], up[16], y[16];
       unpack16(raw[j][0], raw[j][1], g);
       unpack16(raw[j][2], raw[j][3], up);
+      const uint32_t gw[8] = {raw[j][0].x, raw[j][0].y, raw[j][0].z, raw[j][0].w,
+                              raw[j][1].x, raw[j][1].y, raw[j][1].z, raw[j][1].w};
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
-        const float2 sg = bfq_silu2(g[i], g[i + 1]);
+        float2 sg;
+        if constexpr (TABLE) {
+          sg.x = __ldg(silu_tab + (gw[i / 2] & 0xFFFFu));
+          sg.y = __ldg(silu_tab + (gw[i / 2] >> 16));
+        } else {
+          sg = bfq_silu2(g[i], g[i + 1]);
+        }
         const float2 yy = unpack2(mul2_rn(pack2(sg.x, sg.y), pack2(up[i], up[i + 1])));
         y[i] = yy.x;
         y[i + 1] = yy.y;
@@ -330,6 +353,57 @@ extern "C" bfq_status bfq_quant(const void* x, int64_t M, int64_t K, int64_t ld_
   return st;
 }
 
+namespace bfq {
+namespace {
+std::mutex g_silu_mu;
+const float* g_silu_ready[64];  // per device: the built table, or null
+}  // namespace
+
+// The device's silu table, built on first use: the build kernel runs on
+// `stream` and the stream is synchronized once, so that every later call, on
+// any stream, finds the table complete.  Null while the stream is capturing a
+// graph and the table has not been built (the caller then computes silu).
+const float* silu_table(const DeviceInfo& dev, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_silu_mu);
+  if (g_silu_ready[dev.ordinal]) return g_silu_ready[dev.ordinal];
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return nullptr;
+  void* t = nullptr;
+  if (cudaGetSymbolAddress(&t, g_silu_table) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  silu_table_kernel<<<65536 / 256, 256, 0, stream>>>((float*)t);
+  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  g_silu_ready[dev.ordinal] = (const float*)t;
+  return g_silu_ready[dev.ordinal];
+}
+
+namespace {
+
+template <int FMT>
+bfq_status launch_silu_mul_quant(dim3 grid, cudaStream_t s, const __nv_bfloat16* x, int T,
+                                 int I, const int32_t* counts, uint8_t* q, void* scales,
+                                 int64_t scale_ld, const float* tab) {
+  if (tab)
+    return launch_status(launch_pdl(silu_mul_quant_kernel<FMT, true>, grid,
+                                    dim3(kQuantWarps * 32), 0, s, 1, x, T, I, counts, q, scales,
+                                    scale_ld, tab));
+  return launch_status(launch_pdl(silu_mul_quant_kernel<FMT, false>, grid,
+                                  dim3(kQuantWarps * 32), 0, s, 1, x, T, I, counts, q, scales,
+                                  scale_ld, tab));
+}
+
+}  // namespace
+}  // namespace bfq
+
 extern "C" bfq_status bfq_silu_mul_quant(const void* x, int32_t E, int32_t T, int32_t I,
                                          const int32_t* valid_counts, int32_t fmt, void* q,
                                          void* scales, int64_t scale_ld, void* stream) {
@@ -347,24 +421,18 @@ extern "C" bfq_status bfq_silu_mul_quant(const void* x, int32_t E, int32_t T, in
   cudaStream_t s = (cudaStream_t)stream;
   const auto* xb = (const __nv_bfloat16*)x;
   auto* qb = (uint8_t*)q;
+  const float* tab = silu_table(dev, s);
   switch (fmt) {
     case BFQ_SCALE_F32:
-      st = launch_status(launch_pdl(silu_mul_quant_kernel<BFQ_SCALE_F32>, grid,
-                                    dim3(kQuantWarps * 32), 0, s, 1, xb, T, I, valid_counts, qb,
-                                    scales, scale_ld));
-      break;
+      return launch_silu_mul_quant<BFQ_SCALE_F32>(grid, s, xb, T, I, valid_counts, qb, scales,
+                                                  scale_ld, tab);
     case BFQ_SCALE_F32_POW2:
-      st = launch_status(launch_pdl(silu_mul_quant_kernel<BFQ_SCALE_F32_POW2>, grid,
-                                    dim3(kQuantWarps * 32), 0, s, 1, xb, T, I, valid_counts, qb,
-                                    scales, scale_ld));
-      break;
+      return launch_silu_mul_quant<BFQ_SCALE_F32_POW2>(grid, s, xb, T, I, valid_counts, qb,
+                                                       scales, scale_ld, tab);
     default:
-      st = launch_status(launch_pdl(silu_mul_quant_kernel<BFQ_SCALE_UE8M0_PACKED>, grid,
-                                    dim3(kQuantWarps * 32), 0, s, 1, xb, T, I, valid_counts, qb,
-                                    scales, scale_ld));
-      break;
+      return launch_silu_mul_quant<BFQ_SCALE_UE8M0_PACKED>(grid, s, xb, T, I, valid_counts, qb,
+                                                           scales, scale_ld, tab);
   }
-  return st;
 }
 
 extern "C" bfq_status bfq_weight_block_quant(const void* w, int64_t batch, int64_t N,

@@ -130,6 +130,14 @@ bfq_status bfq_quant(const void* x, int64_t M, int64_t K, int64_t ld_x, int32_t 
  * (and all rows of an expert with count <= 0) are neither read nor written,
  * in x, q or scales.
  *
+ * The gate is bf16, so silu has 65536 possible inputs: the library evaluates
+ * silu (the arithmetic above) for all of them once per device into a 256 KB
+ * table in its own device memory, and looks silu up.  The first call on a
+ * device that is not being captured into a CUDA graph builds the table on
+ * `stream` and synchronizes that stream once; calls made while a graph is
+ * being captured before then compute silu in the kernel instead.  Either way
+ * the results are the same, bit for bit.
+ *
  *   x             bf16 [E][T][2I], 16-byte aligned.
  *   E, T, I       E >= 0, T >= 0, I > 0, I % 128 == 0.
  *   valid_counts  device int32 [E]; values are clamped to [0, T].
@@ -328,7 +336,8 @@ bfq_status bfq_interleave_gate_up(const void* w_q, const float* w_scales, int32_
  * bit for bit, without writing h: each 256-wide tile holds a gate block and
  * its up block (weights from bfq_interleave_gate_up), so the epilogue forms
  * y = silu(gate) * up for 128 features of a row and quantizes them as one
- * 1 x 128 group.  Rows r >= count are neither computed nor written (only row
+ * 1 x 128 group (silu from the table described at bfq_silu_mul_quant, built
+ * on the same terms).  Rows r >= count are neither computed nor written (only row
  * tiles below the count are scheduled, as in bfq_gemm_block_fp8_masked).
  *
  *   a_q .. a_scale_ld   as for bfq_gemm_block_fp8_masked (K of the up

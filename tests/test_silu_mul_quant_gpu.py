@@ -70,3 +70,16 @@ def test_silu_mul_quant_large_activations(cuda_lib, orc):
     x = (torch.randn(E, T, 2 * I, generator=g) * 100).to(torch.bfloat16)
     q, sc = _run(bfq, x, counts, 2, 8)
     _check(orc, x, counts, q, sc, 2)
+
+
+@pytest.mark.parametrize("fmt", [0, 2])
+def test_silu_mul_quant_many_experts(cuda_lib, orc, fmt):
+    """More experts than the walk over valid units holds counts for (1100 >
+    1024): the per-block form, one block per pair of rows of an expert."""
+    bfq = cuda_lib
+    E, T, I = 1100, 3, 256
+    g = torch.Generator().manual_seed(17)
+    counts = torch.randint(0, T + 1, (E,), generator=g, dtype=torch.int32)
+    x = synth.masked_activation(E, T, 2 * I, counts, seed=18)
+    q, sc = _run(bfq, x, counts, fmt, 4)
+    _check(orc, x, counts, q, sc, fmt)
