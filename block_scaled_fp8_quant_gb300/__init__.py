@@ -73,6 +73,9 @@ def load_library(build: bool = True):
             "bfq_gemm_block_fp8_noalloc": (I32, [P, P, I32, I64, P, P, I64, I64, I64, P, P]),
             "bfq_gemm_block_fp8_quant": (I32, [P, P, I32, I64, P, P, I64, I64, I64, P, I32, P, P,
                                               I64, P, SZ, P]),
+            "bfq_gemm_block_fp8_ue8m0": (I32, [P, P, I32, I64, P, P, I64, I64, I64, P, P]),
+            "bfq_gemm_block_fp8_masked_ue8m0": (I32, [P, P, I32, I64, P, P, P, I32, I32, I64,
+                                                      I64, P, P]),
             "bfq_interleave_gate_up": (I32, [P, P, I32, I64, I64, P, P, P]),
             "bfq_gemm_block_fp8_masked_silu_quant": (I32, [P, P, I32, I64, P, P, P, I32, I32, I64,
                                                           I64, I32, P, P, I64, P]),
@@ -267,6 +270,28 @@ def bfq_gemm_block_fp8_masked(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w
                                          _stream(stream)))
 
 
+def bfq_gemm_block_fp8_ue8m0(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w_scales, out,
+                             stream=None) -> None:
+    """Dense GEMM for power-of-two scales on the tensor cores' block scaling."""
+    lib = load_library()
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    _check("bfq_gemm_block_fp8_ue8m0",
+           lib.bfq_gemm_block_fp8_ue8m0(_ptr(a_q), _ptr(a_scales), a_fmt, a_scale_ld, _ptr(w_q),
+                                        _ptr(w_scales), M, N, K, _ptr(out), _stream(stream)))
+
+
+def bfq_gemm_block_fp8_masked_ue8m0(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q, w_scales,
+                                    valid_counts, out, stream=None) -> None:
+    lib = load_library()
+    E, T, K = a_q.shape
+    N = w_q.shape[1]
+    _check("bfq_gemm_block_fp8_masked_ue8m0",
+           lib.bfq_gemm_block_fp8_masked_ue8m0(_ptr(a_q), _ptr(a_scales), a_fmt, a_scale_ld,
+                                               _ptr(w_q), _ptr(w_scales), _ptr(valid_counts), E,
+                                               T, N, K, _ptr(out), _stream(stream)))
+
+
 def bfq_poll_device_status(stream=None) -> int:
     return int(load_library().bfq_poll_device_status(_stream(stream)))
 
@@ -347,6 +372,30 @@ def gemm(a_q, a_scales, a_fmt: int, w_q, w_scales, out=None, workspace=None, str
         workspace = gemm_workspace(M, N, K, a_q.device)
     bfq_gemm_block_fp8(a_q, a_scales, a_fmt, a_scales.shape[-1], w_q, w_scales, out,
                        workspace, stream=stream)
+    return out
+
+
+def gemm_ue8m0(a_q, a_scales, a_fmt: int, w_q, w_scales, out=None, stream=None):
+    """out[M, N] (bf16) = block-scaled A * W^T for power-of-two scales, the
+    scales applied by the MMA's block scaling."""
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a_q.device)
+    bfq_gemm_block_fp8_ue8m0(a_q, a_scales, a_fmt, a_scales.shape[-1], w_q, w_scales, out,
+                             stream=stream)
+    return out
+
+
+def gemm_masked_ue8m0(a_q, a_scales, a_fmt: int, w_q, w_scales, valid_counts, out=None,
+                      stream=None):
+    """Masked form of gemm_ue8m0; rows r >= valid_counts[e] are not written."""
+    E, T, K = a_q.shape
+    N = w_q.shape[1]
+    if out is None:
+        out = torch.empty((E, T, N), dtype=torch.bfloat16, device=a_q.device)
+    bfq_gemm_block_fp8_masked_ue8m0(a_q, a_scales, a_fmt, a_scales.shape[-1], w_q, w_scales,
+                                    valid_counts, out, stream=stream)
     return out
 
 

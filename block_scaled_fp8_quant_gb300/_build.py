@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbfq.so")
-SOURCES = ["bfq_api.cu", "quant_kernels.cu", "gemm_kernels.cu"]
+SOURCES = ["bfq_api.cu", "quant_kernels.cu", "gemm_kernels.cu", "gemm_blockscaled.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

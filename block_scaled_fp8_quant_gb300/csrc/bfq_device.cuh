@@ -13,6 +13,17 @@
 
 namespace bfq {
 
+// ---------------------------------------------------------------------------
+// host: TMA tensor maps (defined in gemm_kernels.cu)
+// ---------------------------------------------------------------------------
+// 2D map over a row-major byte matrix [rows][inner] with a 128 x box_rows box
+// and 128-byte swizzling; out-of-range rows read as zero.
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+              uint32_t box_rows);
+// 2D map over the bf16 output [rows][cols] with a 64 x 128 box and 128-byte
+// swizzling, for TMA stores of a staged tile.
+bool make_out_map(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows);
+
 // Kernels whose bounded waits give up latch BFQ_ERR_TIMEOUT into the
 // library's device status word (its address is a kernel argument, see
 // device_status_ptr()); bfq_poll_device_status() reads and clears it.
@@ -284,7 +295,7 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 // with 128-byte swizzling: rows of 128 bytes, 8-row (1024-byte) swizzle atoms
 // stacked along M/N (stride byte offset 1024), descriptor version 1, layout
 // type SWIZZLE_128B.  The tile base must be 1024-byte aligned.
-__device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
+__host__ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address      [0,14)
   d |= (uint64_t)1 << 16;                     // leading byte offset (unused) [16,30)
@@ -302,6 +313,58 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
          | (0u << 10)                   // B format: e4m3
          | ((uint32_t)(N >> 3) << 17)   // N >> 3
          | ((uint32_t)(M >> 4) << 24);  // M >> 4
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4.block_scale: A and B
+// e4m3, both K-major, M x N tile, fp32 accumulator, UE8M0 scale factors;
+// sf_byte (0..3) selects which byte of A's and of B's 32-bit scale words in
+// TMEM this MMA applies (scale_vec::1X: one scale per row for its K = 32).
+__host__ __device__ constexpr uint32_t idesc_e4m3_bs(int M, int N, uint32_t sf_byte) {
+  return (sf_byte << 4)                 // B scale-factor byte    [4,6)
+         | (0u << 7)                    // A format: e4m3         [7,10)
+         | (0u << 10)                   // B format: e4m3         [10,13)
+         | ((uint32_t)(N >> 3) << 17)   // N >> 3                 [17,23)
+         | (1u << 23)                   // scale factors UE8M0    [23]
+         | ((uint32_t)(M >> 4) << 24)   // M >> 4                 [24,29)
+         | (sf_byte << 29);             // A scale-factor byte    [29,31)
+}
+
+// D[tmem] (+)= (A[smem] * 2^(sA - 127)) * (B[smem] * 2^(sB - 127))^T for one
+// K = 32 step, sA / sB the UE8M0 scale of each row of A / B: the selected
+// byte of the 32-bit words at TMEM columns sfa.. / sfb.. (M = 128 rows of A:
+// row 32 c + r at lane r of column sfa + c; N rows of B likewise from sfb),
+// issued by a single thread.
+__device__ __forceinline__ void umma_e4m3_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor of a tcgen05.cp source of 16-byte rows: row r at
+// byte 16 r, i.e. 8-row (128-byte) core matrices stacked contiguously
+// (stride byte offset 128), one core matrix along K (leading byte offset
+// unused), no swizzle, descriptor version 1.  16-byte aligned base.
+__host__ __device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address      [0,14)
+  d |= (uint64_t)(128 >> 4) << 32;            // stride byte offset [32,46)
+  d |= (uint64_t)1 << 46;                     // version            [46,48)
+  return d;                                   // layout type 0: no swizzle
+}
+
+// Copy 32 rows x 128 bits from shared memory (descriptor above) into 4
+// consecutive TMEM columns of lanes 0-31, replicated into each of the four
+// 32-lane quarters (lane 32 q + r, column c = bytes 16 r + 4 c .. + 3 of the
+// source).  Asynchronous; ordered before later tcgen05.mma of this thread.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by a single thread.

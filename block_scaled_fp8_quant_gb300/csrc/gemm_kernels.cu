@@ -32,13 +32,10 @@
 #include <mutex>
 
 #include "bfq_device.cuh"
+#include "gemm_common.cuh"
 
 namespace bfq {
 
-constexpr int kBM = 128;  // rows of A per tile (UMMA M)
-constexpr int kBK = 128;  // K per stage = one scale block
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
-constexpr int kMaxSplits = 8;  // K splits of a tile form one (portable-size) cluster
 
 // BN = 256: three warpgroups.  Warpgroup 0 (warps 0-3) holds the TMA
 // producer (warp 0) and the MMA issuer (warp 1) and gives registers away
@@ -70,37 +67,7 @@ struct GemmCfg {
       (size_t)kStages * kStageBytes + kScaleBytes + kBarrierBytes + 1024;
 };
 
-struct GemmParams {
-  const void* sa;          // activation scales (format a_fmt), column-major
-  int64_t sa_ld;           // leading dimension of sa
-  int64_t sa_estride;      // elements of sa per expert (masked)
-  const float* sw;         // weight scales [nblk][KB]
-  int64_t sw_estride;      // floats of sw per expert (masked)
-  __nv_bfloat16* out;      // [rows][N]
-  int64_t out_estride;     // elements of out per expert (masked)
-  const int32_t* counts;   // masked: per-expert valid rows
-  int* status;             // device error latch
-  int M;                   // dense: rows of A; masked: rows per expert (T)
-  int N, K;
-  int m_tiles, n_tiles, splits;
-  int a_fmt;
-  int E;                   // masked: experts
-  // fused output quant (QOUT kernels): the bf16-rounded output quantized per
-  // 1 x 128 group into q_out (e4m3 [M][N]) and q_scales (format q_fmt,
-  // column-major, leading dimension q_scale_ld); out may then be null.
-  uint8_t* q_out;
-  void* q_scales;
-  int64_t q_scale_ld;
-  int q_fmt;
-  // fused silu-mul-quant (SILU kernel): silu of every bf16 gate, indexed by
-  // its 16 bits (the library's table), or null to compute it
-  const float* silu_tab;
-};
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
 // Fused output quant of one row's 128 accumulated columns, which form exactly
 // one 1 x 128 group (the tile's column halves start at multiples of 128): the
@@ -583,7 +550,6 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
 // — so padding costs no CTA time and the valid tiles spread evenly over the
 // SMs; rows past the count are never written.
 // ----------------------------------------------------------------------------
-constexpr int kPersistMaxExperts = 1024;
 
 // STAGES: depth of the operand ring.  The shared memory a fourth stage would
 // take holds three more output boxes instead, so the staging buffer holds one
@@ -612,35 +578,6 @@ struct PersistCfgT {
 using PersistCfg = PersistCfgT<4>;
 static_assert(PersistCfgT<3>::kSmemBytes == PersistCfgT<4>::kSmemBytes, "same footprint");
 
-// Tile t of the persistent schedule -> (expert, first row, first column,
-// valid rows of the expert).  Masked: tpre[e] = tiles of experts < e,
-// cnt[e] = clamped valid rows of expert e.
-template <bool MASKED>
-__device__ __forceinline__ void persist_tile(int t, const GemmParams& p, const int* tpre,
-                                             const int* cnt, int& e, int& m0, int& n0,
-                                             int& m_limit) {
-  if (MASKED) {
-    int lo = 0, hi = p.E;  // tpre[lo] <= t < tpre[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (tpre[mid] <= t) lo = mid;
-      else hi = mid;
-    }
-    e = lo;
-    m_limit = cnt[e];
-    const int a = (m_limit + kBM - 1) / kBM;  // active row tiles of expert e
-    const int r = t - tpre[e];
-    const int nt = r / a;
-    m0 = (r - nt * a) * kBM;
-    n0 = nt * 256;
-  } else {
-    e = 0;
-    m_limit = p.M;
-    const int nt = t / p.m_tiles;
-    m0 = (t - nt * p.m_tiles) * kBM;
-    n0 = nt * 256;
-  }
-}
 
 template <bool MASKED, bool QOUT = false, bool SILU = false, int STAGES = 4>
 __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
@@ -674,36 +611,7 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int KB = p.K / kBK;
 
-  if (MASKED) {
-    // per-expert tile counts, then an exclusive prefix sum by warp 0
-    griddep_wait();  // the counts may come from the previous kernel
-    for (int x = threadIdx.x; x < p.E; x += blockDim.x) {
-      int c = __ldg(p.counts + x);
-      c = c < 0 ? 0 : (c > p.M ? p.M : c);
-      cnt[x] = c;
-      tpre[x + 1] = (c + kBM - 1) / kBM * p.n_tiles;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int per = (p.E + 31) / 32;
-      const int b = lane * per;
-      const int b_end = min(p.E, b + per);
-      int sum = 0;
-      for (int x = b; x < b_end; ++x) sum += tpre[x + 1];
-      int inc = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-        if (lane >= o) inc += y;
-      }
-      int run = inc - sum;
-      for (int x = b; x < b_end; ++x) {
-        run += tpre[x + 1];
-        tpre[x + 1] = run;
-      }
-      if (lane == 0) tpre[0] = 0;
-    }
-  }
+  if (MASKED) masked_tile_prefix(p, tpre, cnt);
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -1088,9 +996,9 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
 // host side
 // ----------------------------------------------------------------------------
 namespace {
-
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+}  // namespace
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   std::call_once(g_encode_once, [] {
@@ -1137,6 +1045,8 @@ bool make_out_map(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows) {
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 struct Plan {
   int bn = 256;

@@ -309,6 +309,46 @@ bfq_status bfq_gemm_block_fp8_masked(const void* a_q, const void* a_scales, int3
                                      size_t workspace_bytes, void* stream);
 
 /*
+ * Dense block-scaled FP8 GEMM for power-of-two (UE8M0) scales, the scales
+ * applied by the tensor cores' block scaling instead of promotion ([DG-bench]
+ * §4.1–4.2: UE8M0 is the hardware-friendly scale form, each 1 x 128 scale
+ * reused by the four K = 32 MMAs of its block).  Same result definition as
+ * bfq_gemm_block_fp8: multiplying by a power of two is exact, so the two
+ * differ only in fp32 summation order (within the same error bound).
+ * tcgen05.mma kind::mxf8f6f4.block_scale scales each K = 32 step's products
+ * by 2^(eA + eB) and accumulates the whole K range in TMEM; the scale words
+ * are copied into TMEM once per four K blocks.  One CTA per SM walks the
+ * 128 x 256 output tiles; there is no K split.
+ *
+ *   a_q, a_scale_ld, w_q, M, N, K, out   as for bfq_gemm_block_fp8.
+ *   a_fmt          BFQ_SCALE_UE8M0_PACKED or BFQ_SCALE_F32_POW2 (else FORMAT).
+ *   a_scales       column-major, as for bfq_gemm_block_fp8.
+ *   w_scales       float [ceil(N/128)][K/128], each a positive power of two
+ *                  2^-126 .. 2^127 (as bfq_weight_block_quant writes them with
+ *                  fmt = BFQ_SCALE_F32_POW2).
+ * A scale that is not a positive power of two cannot be applied: the kernel
+ * latches BFQ_ERR_FORMAT in the device status (bfq_poll_device_status) and
+ * the output of that call is undefined.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, FORMAT, CUDA, DEVICE.
+ */
+bfq_status bfq_gemm_block_fp8_ue8m0(const void* a_q, const void* a_scales, int32_t a_fmt,
+                                    int64_t a_scale_ld, const void* w_q, const float* w_scales,
+                                    int64_t M, int64_t N, int64_t K, void* out, void* stream);
+
+/*
+ * Masked grouped form of bfq_gemm_block_fp8_ue8m0 (the per-expert valid-row
+ * counts of bfq_gemm_block_fp8_masked, whose argument rules apply, without
+ * its unused expected_m and workspace): rows r >= valid_counts[e] are never
+ * written; a_fmt and w_scales as for bfq_gemm_block_fp8_ue8m0; E <= 1024.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, FORMAT, CUDA, DEVICE.
+ */
+bfq_status bfq_gemm_block_fp8_masked_ue8m0(const void* a_q, const void* a_scales, int32_t a_fmt,
+                                           int64_t a_scale_ld, const void* w_q,
+                                           const float* w_scales, const int32_t* valid_counts,
+                                           int32_t E, int32_t T, int64_t N, int64_t K,
+                                           void* out, void* stream);
+
+/*
  * Reorders an MoE up-projection weight for the fused form below: each
  * expert's [2I][K] e4m3 weight (gate rows 0..I-1, up rows I..2I-1, the
  * split of "[EP+DP] Optimize the little operations in the DeepGEMM + DeepEP
