@@ -114,6 +114,11 @@ __device__ __forceinline__ float bfq_silu(float g) {
   return __fdiv_rn(g, __fadd_rn(1.0f, bfq_expf(-g)));
 }
 
+// Bring the 128-byte line holding p into L2 (no register result, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // 16-byte streaming load that does not allocate in L1.
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;

@@ -227,67 +227,136 @@ __global__ void __launch_bounds__(BsCfg::kThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------------ scale loader ------------------------------
-    const bool packed = p.a_fmt == BFQ_SCALE_UE8M0_PACKED;
-    const int nblks = (p.N + 127) / 128;
+    // Group q (tile q / gpt, K blocks 4 (q mod gpt) ..) is fetched into
+    // registers (all of its global loads issued together) several groups
+    // ahead of the one written to shared memory, the register sets rotating.
+    const int gpt = (KB + C::kGroup - 1) / C::kGroup;
+    const int ngroups = my_tiles * gpt;
+    int cur_tt = -1, e = 0, m0 = 0, n0 = 0, ml = 0;
     bool bad = false;
-    int q = 0;
-    for (int tt = 0; tt < my_tiles; ++tt) {
-      int e, m0, n0, ml;
-      persist_tile<MASKED>(blockIdx.x + tt * gridDim.x, p, tpre, cnt, e, m0, n0, ml);
+    struct Fetched {
+      uint32_t a[16];  // packed: a[c] = word of row 32 c + lane; pow2: a[4 c + k] = fp32 bits
+      uint32_t w;      // lane j < 8: fp32 bits of weight block nb0 + j / 4, K block i0 + j % 4
+      int nk;          // K blocks in this group
+    };
+    auto fetch = [&](int q, Fetched& f) {
+      const int tt = q / gpt;
+      const int i0 = (q - tt * gpt) * C::kGroup;
+      if (tt != cur_tt) {
+        cur_tt = tt;
+        persist_tile<MASKED>(blockIdx.x + tt * gridDim.x, p, tpre, cnt, e, m0, n0, ml);
+      }
       const uint32_t* sa = (const uint32_t*)p.sa + (MASKED ? (int64_t)e * p.sa_estride : 0);
       const float* sw = p.sw + (MASKED ? (int64_t)e * p.sw_estride : 0);
-      const int nb0 = n0 / 128;
-      bool stop = false;
-      for (int i0 = 0; i0 < KB; i0 += C::kGroup, ++q) {
-        const int slot = q % C::kSfSlots;
-        if (!mbar_wait(&sempty[slot], ((uint32_t)(q / C::kSfSlots) & 1u) ^ 1u, abort_flag,
-                       p.status, kWaitTimeoutNs)) {
-          stop = true;
-          break;
-        }
-        uint32_t* wa = sf + slot * C::kSfSlotWords;
-        uint32_t* wb = wa + C::kSfaWords;
-        const int nk = min(C::kGroup, KB - i0);
-        // activation row 32 c + lane -> word 4 lane + c (the copy puts bytes
-        // 16 r + 4 c of the source at lane r, column c)
+      f.nk = min(C::kGroup, KB - i0);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int m = m0 + c * 32 + lane;
-          uint32_t w = 0;
-          if (m < ml) {
-            if (packed) {
-              w = __ldg(sa + (int64_t)(i0 >> 2) * p.sa_ld + m);
-            } else {
-              for (int k = 0; k < nk; ++k) {
-                const uint32_t b = __ldg(sa + (int64_t)(i0 + k) * p.sa_ld + m);
-                bad |= !pow2_bits(b);
-                w |= ((b >> 23) & 0xFFu) << (8 * k);
-              }
-            }
-          }
-          wa[lane * 4 + c] = w;
-        }
-        // weight rows: one word per 128-row block, the same for all its rows
-        uint32_t wv[2];
+      for (int c = 0; c < 4; ++c) {
+        const int m = m0 + c * 32 + lane;
+        if (p.a_fmt == BFQ_SCALE_UE8M0_PACKED) {
+          f.a[c] = m < ml ? __ldg(sa + (int64_t)(i0 >> 2) * p.sa_ld + m) : 0u;
+        } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t w = 0;
-          if (nb0 + h < nblks) {
-            for (int k = 0; k < nk; ++k) {
-              const uint32_t b = __float_as_uint(__ldg(sw + (int64_t)(nb0 + h) * KB + i0 + k));
-              bad |= !pow2_bits(b);
-              w |= ((b >> 23) & 0xFFu) << (8 * k);
-            }
-          }
-          wv[h] = w;
+          for (int k = 0; k < 4; ++k)
+            f.a[4 * c + k] =
+                (m < ml && k < f.nk) ? __ldg(sa + (int64_t)(i0 + k) * p.sa_ld + m) : 0x3F800000u;
         }
-#pragma unroll
-        for (int j = lane; j < C::kSfbWords; j += 32) wb[j] = wv[j >> 7];
-        fence_proxy_async_smem();  // visible to the tensor cores' copy
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sfull[slot]);
       }
-      if (stop) break;
+      const int nb = n0 / 128 + (lane >> 2), kb = i0 + (lane & 3);
+      f.w = (lane < 8 && nb < (p.N + 127) / 128 && kb < KB)
+                ? __float_as_uint(__ldg(sw + (int64_t)nb * KB + kb))
+                : 0x3F800000u;
+    };
+    // The scale lines of group q + kPrefetchGroups are pulled into L2 while
+    // group q is fetched: behind a full operand stream a scale line that
+    // missed L2 would otherwise cost an HBM round trip per group.
+    constexpr int kPrefetchGroups = 8;
+    int pf_tt = -1, pf_e = 0, pf_m0 = 0, pf_n0 = 0, pf_ml = 0;
+    auto prefetch_group = [&](int q) {
+      const int tt = q / gpt;
+      const int i0 = (q - tt * gpt) * C::kGroup;
+      if (tt != pf_tt) {
+        pf_tt = tt;
+        persist_tile<MASKED>(blockIdx.x + tt * gridDim.x, p, tpre, cnt, pf_e, pf_m0, pf_n0, pf_ml);
+      }
+      const uint32_t* sa = (const uint32_t*)p.sa + (MASKED ? (int64_t)pf_e * p.sa_estride : 0);
+      const float* sw = p.sw + (MASKED ? (int64_t)pf_e * p.sw_estride : 0);
+      const int nk = min(C::kGroup, KB - i0);
+      if (p.a_fmt == BFQ_SCALE_UE8M0_PACKED) {
+        // four 128-byte lines: rows 32 lane .. of the group's word column
+        if (lane < 4 && pf_m0 + 32 * lane < pf_ml)
+          prefetch_l2(sa + (int64_t)(i0 >> 2) * p.sa_ld + pf_m0 + 32 * lane);
+      } else if (lane < 16 && (lane >> 2) < nk && pf_m0 + 32 * (lane & 3) < pf_ml) {
+        prefetch_l2(sa + (int64_t)(i0 + (lane >> 2)) * p.sa_ld + pf_m0 + 32 * (lane & 3));
+      }
+      const int nb = pf_n0 / 128 + ((lane - 16) >> 2), kb = i0 + (lane & 3);
+      if (lane >= 16 && lane < 24 && nb < (p.N + 127) / 128 && (lane & 3) < nk)
+        prefetch_l2(sw + (int64_t)nb * KB + kb);
+    };
+    auto emit = [&](int q, const Fetched& f) -> bool {
+      const int slot = q % C::kSfSlots;
+      // lane 0 waits and the warp takes its decision together (the shuffles
+      // below need every lane)
+      bool ok = true;
+      if (lane == 0)
+        ok = mbar_wait(&sempty[slot], ((uint32_t)(q / C::kSfSlots) & 1u) ^ 1u, abort_flag,
+                       p.status, kWaitTimeoutNs);
+      if (!__shfl_sync(0xFFFFFFFFu, (int)ok, 0)) return false;
+      __syncwarp();
+      uint32_t* wa = sf + slot * C::kSfSlotWords;
+      uint32_t* wb = wa + C::kSfaWords;
+      // activation row 32 c + lane -> word 4 lane + c (the copy puts bytes
+      // 16 r + 4 c of the source at lane r, column c)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w = f.a[c];
+        if (p.a_fmt != BFQ_SCALE_UE8M0_PACKED) {
+          w = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t b = f.a[4 * c + k];
+            bad |= !pow2_bits(b);
+            w |= k < f.nk ? ((b >> 23) & 0xFFu) << (8 * k) : 0u;
+          }
+        }
+        wa[lane * 4 + c] = w;
+      }
+      // weight rows: one word per 128-row block, the same for all its rows
+      if (lane < 8) bad |= !pow2_bits(f.w);
+      uint32_t wv0 = 0, wv1 = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, f.w, k);
+        const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, f.w, 4 + k);
+        if (k < f.nk) {
+          wv0 |= ((b0 >> 23) & 0xFFu) << (8 * k);
+          wv1 |= ((b1 >> 23) & 0xFFu) << (8 * k);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < C::kSfbWords / 32; ++j) wb[lane + 32 * j] = j < 4 ? wv0 : wv1;
+      fence_proxy_async_smem();  // visible to the tensor cores' copy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfull[slot]);
+      return true;
+    };
+    // kFetchAhead groups' loads in flight while one is written (under a
+    // full operand stream an L2 hit takes ~2 us, four K blocks of MMA less)
+    constexpr int kFetchAhead = 3;
+    Fetched f[kFetchAhead + 1];
+    for (int q = 0; q < kPrefetchGroups && q < ngroups; ++q) prefetch_group(q);
+#pragma unroll
+    for (int d = 0; d < kFetchAhead; ++d)
+      if (d < ngroups) fetch(d, f[d]);
+    bool stop = false;
+    for (int q0 = 0; q0 < ngroups && !stop; q0 += kFetchAhead + 1) {
+#pragma unroll
+      for (int d = 0; d <= kFetchAhead; ++d) {
+        const int q = q0 + d;
+        if (stop || q >= ngroups) continue;
+        if (q + kPrefetchGroups < ngroups) prefetch_group(q + kPrefetchGroups);
+        if (q + kFetchAhead < ngroups) fetch(q + kFetchAhead, f[(d + kFetchAhead) % (kFetchAhead + 1)]);
+        stop = !emit(q, f[d]);
+      }
     }
     if (bad) atomicCAS(p.status, 0, BFQ_ERR_FORMAT);
   } else if (warp >= C::kEpiWarp0) {
