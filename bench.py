@@ -650,6 +650,53 @@ def gated_times(torch, fn, reps):
     return ts[len(ts) // 2]
 
 
+def measure_ue8m0_arms(bfq, torch, dev, fp8_peak, ms=(1024, 4096)):
+    """Dense GEMM with UE8M0 scales on both operands (packed activation
+    scales, power-of-two 128x128 weight scales; the sweep's (n, k) shapes):
+    the block-scaled arm (bfq_gemm_block_fp8_ue8m0, scales applied by the
+    MMA) against the promotion kernel (bfq_gemm_block_fp8) on the same
+    inputs, back to back in one CUDA graph over weight copies holding 2.5x
+    the L2.  The two results agree to within summation order."""
+    import bfq_synth as synth
+
+    rows = []
+    for n, k in SWEEP_NK:
+        w = synth.weight(n, k, seed=n + k + 5, device=dev)
+        wq, sw = bfq.weight_block_quant(w, bfq.SCALE_F32_POW2)
+        del w
+        copies = max(2, -(-int(2.5 * L2_BYTES) // (n * k)))
+        wqs = [wq] + [wq.clone() for _ in range(copies - 1)]
+        sws = [sw] + [sw.clone() for _ in range(copies - 1)]
+        for m in ms:
+            x = synth.activation(m, k, seed=m + n + 5, device=dev)
+            q, s = bfq.quant(x, bfq.SCALE_UE8M0_PACKED)
+            o_bs = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+            o_pr = torch.empty_like(o_bs)
+            t_bs = graph_back_to_back_us(
+                torch, lambda i: bfq.bfq_gemm_block_fp8_ue8m0(q, s, 2, s.shape[-1], wqs[i], sws[i],
+                                                              o_bs), copies, max(4 * copies, 16))
+            t_pr = graph_back_to_back_us(
+                torch, lambda i: bfq.bfq_gemm_block_fp8(q, s, 2, s.shape[-1], wqs[i], sws[i], o_pr,
+                                                        None), copies, max(4 * copies, 16))
+            torch.cuda.synchronize()
+            diff = (o_bs.float() - o_pr.float()).abs().max().item()
+            scale = o_pr.float().abs().max().item()
+            fl = 2.0 * m * n * k
+            rows.append({"m": m, "n": n, "k": k, "block_scaled_us": round(t_bs, 2),
+                         "promotion_us": round(t_pr, 2), "speedup": round(t_pr / t_bs, 3),
+                         "block_scaled_tflops": round(fl / t_bs / 1e6, 1),
+                         "block_scaled_frac_fp8": round(fl / t_bs / 1e6 / fp8_peak, 3),
+                         "promotion_tflops": round(fl / t_pr / 1e6, 1),
+                         "max_abs_diff_rel": float(f"{diff / max(scale, 1e-30):.2e}")})
+            del q, s, o_bs, o_pr, x
+        del wqs, sws, wq, sw
+        torch.cuda.empty_cache()
+    return {"timing": "back to back in one CUDA graph over weight copies holding 2.5x the L2",
+            "plan": "bfq_gemm_block_fp8_ue8m0 runs the promotion plan for M <= 128, K < 1024 or "
+                    "fewer tiles than half the SMs",
+            "shapes": rows}
+
+
 def graph_back_to_back_us(torch, fn, copies, calls, trials=5):
     """Per-call device time (us) of fn(i) issued back to back, i cycling over
     `copies` operand sets, as one CUDA graph (no host launch gaps; each launch
@@ -802,31 +849,47 @@ def measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, reps):
     sa_dn = torch.empty((E, bfq.scale_cols(I, 2), T), dtype=torch.int32, device=dev)
     out = torch.empty((E, T, H), dtype=torch.bfloat16, device=dev)
 
+    # UE8M0 scales on both operands: the GEMMs run on the block-scaled arm
+    # (scales applied by the MMA), measured faster here than promotion,
+    # which is timed beside it
     def up():
-        bfq.bfq_gemm_block_fp8_masked(a_up, sa_up, 2, T, w_up, s_up, d_counts, h)
+        bfq.bfq_gemm_block_fp8_masked_ue8m0(a_up, sa_up, 2, T, w_up, s_up, d_counts, h)
 
     def act():
         bfq.bfq_silu_mul_quant(h, d_counts, a_dn, sa_dn, 2, T)
 
     def down():
+        bfq.bfq_gemm_block_fp8_masked_ue8m0(a_dn, sa_dn, 2, T, w_dn, s_dn, d_counts, out)
+
+    def up_promotion():
+        bfq.bfq_gemm_block_fp8_masked(a_up, sa_up, 2, T, w_up, s_up, d_counts, h)
+
+    def down_promotion():
         bfq.bfq_gemm_block_fp8_masked(a_dn, sa_dn, 2, T, w_dn, s_dn, d_counts, out)
 
-    for fn in (up, act, down):
+    for fn in (up_promotion, act, down_promotion, up, act, down):
         fn()
     torch.cuda.synchronize()
     active = int((counts > 0).sum())
     res = {"experts": E, "t_max": T, "valid_rows": tot, "active_experts": active}
-    for name, fn, n, k in (("up_gemm", up, 2 * I, H), ("down_gemm", down, H, I)):
+    for name, fn, fn_pr, n, k in (("up_gemm", up, up_promotion, 2 * I, H),
+                                  ("down_gemm", down, down_promotion, H, I)):
         us = gated_times(torch, fn, reps)
+        us_b2b = graph_back_to_back_us(torch, lambda i, fn=fn: fn(), 1, 8)
+        us_pr = gated_times(torch, fn_pr, reps)
+        us_pr_b2b = graph_back_to_back_us(torch, lambda i, fn=fn_pr: fn(), 1, 8)
         flops = 2.0 * tot * n * k
         nbytes = active * n * k + tot * k + 2 * tot * n + active * (n // 128) * (k // 128) * 4 \
             + tot * (k // 512) * 4
         t_roof = max(flops / (fp8_peak * 1e12), nbytes / (hbm_peak * 1e9))
-        res[name] = {"n": n, "k": k, "us": round(us, 2), "tflops": round(flops / us / 1e6, 1),
+        res[name] = {"n": n, "k": k, "arm": "block_scaled", "us": round(us, 2),
+                     "us_b2b": round(us_b2b, 2), "tflops": round(flops / us / 1e6, 1),
                      "gbps": round(nbytes / (us * 1e-6) / 1e9, 1),
                      "roofline_frac": round(t_roof * 1e6 / us, 3),
+                     "roofline_frac_b2b": round(t_roof * 1e6 / us_b2b, 3),
                      "bound": "tensor" if flops / (fp8_peak * 1e12) > nbytes / (hbm_peak * 1e9)
-                     else "hbm"}
+                     else "hbm",
+                     "promotion_us": round(us_pr, 2), "promotion_us_b2b": round(us_pr_b2b, 2)}
     us = gated_times(torch, act, reps)
     nbytes = tot * (2 * I * 2 + I) + tot * (I // 512) * 4
     gbs = nbytes / (us * 1e-6) / 1e9
@@ -853,7 +916,8 @@ def measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, reps):
     torch.cuda.synchronize()
     us_fused = gated_times(torch, up_act_fused, reps)
     us_seq = {}
-    for name, fns in (("unfused", (up, act, down)), ("fused", (up_act_fused, down))):
+    for name, fns in (("unfused", (up, act, down)), ("fused", (up_act_fused, down)),
+                      ("unfused_promotion", (up_promotion, act, down_promotion))):
         def chain(i, fns=fns):
             for fn in fns:
                 fn()
@@ -1049,6 +1113,7 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         line["quant_sweep"] = measure_quant_sweep(bfq, torch, dev, hbm_peak, 10)
         line["moe_slice"] = measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, 10)
+        line["ue8m0_arms"] = measure_ue8m0_arms(bfq, torch, dev, fp8_peak)
         line["fused_output_quant"] = measure_fused_quant(bfq, torch, dev, hbm_peak)
         if bfq.bfq_poll_device_status() != 0:
             raise RuntimeError("device watchdog fired during the extra measurements")

@@ -508,6 +508,14 @@ extern "C" bfq_status bfq_gemm_block_fp8_ue8m0(const void* a_q, const void* a_sc
   DeviceInfo dev;
   bfq_status st = check_device_bs(&dev);
   if (st != BFQ_OK) return st;
+  // Launch plan: with one row tile, K < 1024 or fewer than half as many
+  // tiles as SMs the promotion kernel's plan (K split over a cluster,
+  // double-buffered accumulators) is faster (measured); it computes the same
+  // result.
+  const int64_t tiles = cdiv(M, kBM) * cdiv(N, BsCfg::kBN);
+  if (M <= kBM || K < 1024 || 2 * tiles < dev.sm_count)
+    return bfq_gemm_block_fp8(a_q, a_scales, a_fmt, a_scale_ld, w_q, w_scales, M, N, K, out,
+                              nullptr, 0, stream);
   CUtensorMap ma, mw, mo;
   if (!make_map(&ma, a_q, (uint64_t)K, (uint64_t)M, kBM) ||
       !make_map(&mw, w_q, (uint64_t)K, (uint64_t)N, (uint32_t)BsCfg::kBN) ||

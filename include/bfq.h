@@ -318,7 +318,10 @@ bfq_status bfq_gemm_block_fp8_masked(const void* a_q, const void* a_scales, int3
  * tcgen05.mma kind::mxf8f6f4.block_scale scales each K = 32 step's products
  * by 2^(eA + eB) and accumulates the whole K range in TMEM; the scale words
  * are copied into TMEM once per four K blocks.  One CTA per SM walks the
- * 128 x 256 output tiles; there is no K split.
+ * 128 x 256 output tiles; there is no K split.  Launch plan: for M <= 128,
+ * K < 1024 or fewer output tiles than half the SMs, the call runs
+ * bfq_gemm_block_fp8's plan instead (promotion; K split over a cluster),
+ * which is faster there and gives the same result for these scales.
  *
  *   a_q, a_scale_ld, w_q, M, N, K, out   as for bfq_gemm_block_fp8.
  *   a_fmt          BFQ_SCALE_UE8M0_PACKED or BFQ_SCALE_F32_POW2 (else FORMAT).

@@ -44,27 +44,51 @@ def _dense_problem(orc, M, N, K, fmt, seed):
     return aq, sa, wq, sw, dev
 
 
-def _check_dense(orc, out, aq, sa, wq, sw, fmt, what):
-    ref = orc.gemm(aq, sa, fmt, wq, sw)
-    an = np.linalg.norm(orc.dequant_rows(aq, sa, fmt), axis=1)
+def _check_dense(orc, out, aq, sa, wq, sw, fmt, what, rows=None):
+    """All rows, or the given sample of rows, within the gate in every column."""
+    r = np.arange(aq.shape[0]) if rows is None else np.asarray(rows)
+    ref = orc.gemm(aq, sa, fmt, wq, sw, rows=r)
+    an = np.linalg.norm(orc.dequant_rows(aq[r], sa[:, r], fmt), axis=1)
     wn = np.linalg.norm(orc.dequant_weight(wq, sw), axis=1)
-    got = out.float().cpu().numpy()
+    got = out.float().cpu().numpy()[r]
     assert_gemm_close(got, ref, an, wn, what)
     return got, ref
 
 
-# (M, N, K): one tile with one group of four K blocks; a partial last group;
-# ragged rows and a half-full last column tile; a single row; a single K
-# block; more tiles than SMs (the persistent walk); long K.
-DENSE = [(128, 256, 512), (128, 256, 640), (200, 320, 1152), (1, 64, 128), (3, 192, 256),
-         (130, 4160, 384), (1024, 8192, 256), (256, 512, 7168), (77, 1088, 2944)]
+def _sample_rows(M, seed):
+    """First and last rows of every 128-row tile plus seeded rows."""
+    rng = np.random.default_rng(seed)
+    tiles = np.arange(0, M, 128)
+    return np.unique(np.concatenate([tiles, np.minimum(tiles + 127, M - 1),
+                                     rng.integers(0, M, 8)]))
+
+
+def _on_block_scaled_plan(M, N, K):
+    """The entry point runs the block-scaled kernel (not the promotion plan
+    it keeps for one row tile, K < 1024 or few tiles)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = -(-M // 128) * -(-N // 256)
+    return M > 128 and K >= 1024 and 2 * tiles >= sms
+
+
+# Block-scaled plan (M, N, K): a partial last group of K blocks (9 = 4+4+1,
+# 23 = 4*5+3); ragged rows (the last tile 1, 80 or 20 rows); a half-full last
+# column tile (N % 256 == 64 or 192); one tile per SM and several per SM.
+BS_PLAN = [(1300, 1856, 1152), (129, 19968, 1024), (1024, 8192, 1024), (2000, 2496, 2944),
+           (4096, 2304, 1536)]
+# Promotion plan through the same entry point: one row tile, K < 1024, few tiles.
+PROMO_PLAN = [(1, 64, 128), (128, 256, 512), (77, 1088, 2944), (256, 512, 640),
+              (1024, 8192, 256)]
 
 
 @pytest.mark.parametrize("fmt", [1, 2])
-@pytest.mark.parametrize("M,N,K", DENSE)
+@pytest.mark.parametrize("M,N,K", BS_PLAN)
 def test_ue8m0_gemm_parity(cuda_lib, orc, fmt, M, N, K):
-    """Packed UE8M0 and fp32 power-of-two activation scales; repeated calls
-    bit-identical; no error latched."""
+    """Packed UE8M0 and fp32 power-of-two activation scales on the
+    block-scaled kernel: sampled rows (every tile's first and last) in every
+    column; repeated calls bit-identical; every element written; no error
+    latched."""
+    assert _on_block_scaled_plan(M, N, K)
     bfq = cuda_lib
     aq, sa, wq, sw, d = _dense_problem(orc, M, N, K, fmt, seed=7 * M + N + K + fmt)
     out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -73,47 +97,69 @@ def test_ue8m0_gemm_parity(cuda_lib, orc, fmt, M, N, K):
     torch.cuda.synchronize()
     assert bfq.bfq_poll_device_status() == 0
     assert torch.equal(out, again), "repeated calls differ"
-    _check_dense(orc, out, aq, sa, wq, sw, fmt, f"ue8m0 {M}x{N}x{K} fmt{fmt}")
+    assert not torch.isnan(out).any(), "output not fully written"
+    _check_dense(orc, out, aq, sa, wq, sw, fmt, f"ue8m0 {M}x{N}x{K} fmt{fmt}",
+                 rows=_sample_rows(M, M + N + K))
+
+
+@pytest.mark.parametrize("M,N,K", PROMO_PLAN)
+def test_ue8m0_entry_on_promotion_plan(cuda_lib, orc, M, N, K):
+    """Shapes the entry point hands to the promotion kernel's plan: same
+    result definition, all rows checked."""
+    assert not _on_block_scaled_plan(M, N, K)
+    bfq = cuda_lib
+    aq, sa, wq, sw, d = _dense_problem(orc, M, N, K, 2, seed=3 * M + N + K)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bfq.gemm_ue8m0(d[0], d[1], 2, d[2], d[3], out=out)
+    torch.cuda.synchronize()
+    assert bfq.bfq_poll_device_status() == 0
+    _check_dense(orc, out, aq, sa, wq, sw, 2, f"ue8m0 entry {M}x{N}x{K}")
 
 
 def test_ue8m0_matches_promotion_kernel(cuda_lib, orc):
     """The same UE8M0 problem through both kernels: both within the gate of
-    the oracle, and within one bf16 ulp (plus 1e-4 of the norms) of each
-    other — only the fp32 summation order differs."""
+    the oracle on sampled rows, and within one bf16 ulp (plus 1e-4 of the
+    norms) of each other everywhere — only the fp32 summation order differs."""
     bfq = cuda_lib
-    M, N, K = 512, 2048, 3072
+    M, N, K = 1024, 2560, 3072
+    assert _on_block_scaled_plan(M, N, K)
     aq, sa, wq, sw, d = _dense_problem(orc, M, N, K, 2, seed=99)
     bs = bfq.gemm_ue8m0(d[0], d[1], 2, d[2], d[3])
     pr = bfq.gemm(d[0], d[1], 2, d[2], d[3])
     torch.cuda.synchronize()
-    got, ref = _check_dense(orc, bs, aq, sa, wq, sw, 2, "block-scaled")
-    _check_dense(orc, pr, aq, sa, wq, sw, 2, "promotion")
+    rows = _sample_rows(M, 99)
+    got, ref = _check_dense(orc, bs, aq, sa, wq, sw, 2, "block-scaled", rows=rows)
+    _check_dense(orc, pr, aq, sa, wq, sw, 2, "promotion", rows=rows)
+    assert calc_diff(got, ref) < 1e-4
     an = np.linalg.norm(orc.dequant_rows(aq, sa, 2), axis=1)
     wn = np.linalg.norm(orc.dequant_weight(wq, sw), axis=1)
+    b = bs.float().cpu().numpy()
     p = pr.float().cpu().numpy()
     slack = 2.0 ** -7 * np.abs(p) + 1e-4 * an[:, None] * wn[None, :]
-    assert (np.abs(got - p) <= slack).all()
-    assert calc_diff(got, ref) < 1e-4
+    assert (np.abs(b - p) <= slack).all()
 
 
 def test_ue8m0_output_rows_only(cuda_lib, orc):
-    """A guard band after the [M][N] output is never written."""
+    """A guard band after the [M][N] output is never written (the last row
+    tile holds 44 rows, clipped by the output tensor map)."""
     bfq = cuda_lib
-    M, N, K = 9, 2048, 1024
+    M, N, K = 300, 6656, 1024
+    assert _on_block_scaled_plan(M, N, K)
     aq, sa, wq, sw, d = _dense_problem(orc, M, N, K, 2, seed=71)
     buf = torch.full(((M + 7) * N,), float("nan"), dtype=torch.bfloat16, device="cuda")
     out = buf[:M * N].view(M, N)
     bfq.gemm_ue8m0(d[0], d[1], 2, d[2], d[3], out=out)
     torch.cuda.synchronize()
     assert torch.isnan(buf[M * N:]).all(), "wrote past the output"
-    _check_dense(orc, out, aq, sa, wq, sw, 2, "guarded")
+    _check_dense(orc, out, aq, sa, wq, sw, 2, "guarded", rows=_sample_rows(M, 71))
 
 
 def test_ue8m0_rejects_non_pow2_formats(cuda_lib, orc):
     """fp32 activation scales are refused on the host; a weight scale that
     is not a power of two is caught on the device (BFQ_ERR_FORMAT latched)."""
     bfq = cuda_lib
-    M, N, K = 64, 256, 512
+    M, N, K = 256, 10240, 1024
+    assert _on_block_scaled_plan(M, N, K)
     aq, sa, wq, sw, d = _dense_problem(orc, M, N, K, 2, seed=5)
     out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     a32 = torch.ones((K // 128, M), dtype=torch.float32, device="cuda")
@@ -130,7 +176,7 @@ def test_ue8m0_rejects_non_pow2_formats(cuda_lib, orc):
     bfq.bfq_gemm_block_fp8_ue8m0(d[0], d[1], 2, d[1].shape[-1], d[2], d[3], out)
     torch.cuda.synchronize()
     assert bfq.bfq_poll_device_status() == 0
-    _check_dense(orc, out, aq, sa, wq, sw, 2, "after a rejected call")
+    _check_dense(orc, out, aq, sa, wq, sw, 2, "after a rejected call", rows=_sample_rows(M, 5))
 
 
 def _expert_problem(orc, E, T, N, K, counts, seed, experts=None):
@@ -201,14 +247,16 @@ def test_ue8m0_masked_more_tiles_than_sms(cuda_lib, orc):
 
 def test_ue8m0_masked_equals_dense_per_expert(cuda_lib, orc):
     """Each expert's valid rows of the masked form equal the dense form of
-    the same kernel on those rows, bit for bit."""
+    the same kernel on those rows, bit for bit (sizes for which the dense
+    entry point runs the block-scaled kernel)."""
     bfq = cuda_lib
-    E, T, N, K = 2, 136, 512, 1024
-    cnt = np.array([136, 45], np.int32)
+    E, T, N, K = 2, 256, 9728, 1024
+    cnt = np.array([136, 200], np.int32)
     aq, sa, wq, sw = _expert_problem(orc, E, T, N, K, cnt, seed=17)
-    out = _run_masked(bfq, orc, aq, sa, wq, sw, cnt)
+    out = _run_masked(bfq, orc, aq, sa, wq, sw, cnt, experts=set(range(E)))
     for e in range(E):
         c = int(cnt[e])
+        assert _on_block_scaled_plan(c, N, K)
         d_sa = torch.from_numpy(sa[e].view(np.int32).copy()).cuda()
         dense = torch.empty((c, N), dtype=torch.bfloat16, device="cuda")
         bfq.bfq_gemm_block_fp8_ue8m0(
