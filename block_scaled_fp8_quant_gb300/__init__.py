@@ -79,6 +79,9 @@ def load_library(build: bool = True):
             "bfq_interleave_gate_up": (I32, [P, P, I32, I64, I64, P, P, P]),
             "bfq_gemm_block_fp8_masked_silu_quant": (I32, [P, P, I32, I64, P, P, P, I32, I32, I64,
                                                           I64, I32, P, P, I64, P]),
+            "bfq_gemm_block_fp8_masked_silu_quant_ue8m0": (I32, [P, P, I32, I64, P, P, P, I32,
+                                                                I32, I64, I64, I32, P, P, I64,
+                                                                P]),
             "bfq_gemm_noalloc_scratch_bytes": (SZ, []),
             "bfq_poll_device_status": (I32, [P]),
             "bfq_set_programmatic_launch": (I32, [I32]),
@@ -225,6 +228,20 @@ def bfq_gemm_block_fp8_masked_silu_quant(a_q, a_scales, a_fmt: int, a_scale_ld: 
     I = w_q.shape[1] // 2
     _check("bfq_gemm_block_fp8_masked_silu_quant",
            lib.bfq_gemm_block_fp8_masked_silu_quant(
+               _ptr(a_q), _ptr(a_scales), a_fmt, a_scale_ld, _ptr(w_q), _ptr(w_scales),
+               _ptr(valid_counts), E, T, I, K, q_fmt, _ptr(q_out), _ptr(q_scales), q_scale_ld,
+               _stream(stream)))
+
+
+def bfq_gemm_block_fp8_masked_silu_quant_ue8m0(a_q, a_scales, a_fmt: int, a_scale_ld: int, w_q,
+                                               w_scales, valid_counts, q_fmt: int, q_out,
+                                               q_scales, q_scale_ld: int, stream=None) -> None:
+    """The fused up projection on the block-scaled kernel (UE8M0 scales)."""
+    lib = load_library()
+    E, T, K = a_q.shape
+    I = w_q.shape[1] // 2
+    _check("bfq_gemm_block_fp8_masked_silu_quant_ue8m0",
+           lib.bfq_gemm_block_fp8_masked_silu_quant_ue8m0(
                _ptr(a_q), _ptr(a_scales), a_fmt, a_scale_ld, _ptr(w_q), _ptr(w_scales),
                _ptr(valid_counts), E, T, I, K, q_fmt, _ptr(q_out), _ptr(q_scales), q_scale_ld,
                _stream(stream)))

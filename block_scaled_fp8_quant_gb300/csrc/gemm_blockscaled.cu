@@ -21,10 +21,11 @@
 //               issues 4 block-scaled MMAs per K block, the scale byte being
 //               the K block's position in its group of four.
 //   warp 2      scale loader: per group of four K blocks, one 32-bit word per
-//               activation row (the packed UE8M0 word as stored, or the
-//               exponent bytes of four fp32 powers of two) and one per weight
-//               row (the exponent bytes of its 128-row block's four fp32
-//               scales), in the row order the copy expects.
+//               activation row (the packed UE8M0 word as stored, brought in
+//               by a bulk copy, or the exponent bytes of four fp32 powers of
+//               two) and one per weight row (the exponent bytes of its
+//               128-row block's four fp32 scales), in the row order the copy
+//               into TMEM expects.
 //   warps 4-11  epilogue: once per tile, read the fp32 accumulator (each warp
 //               32 rows x 128 columns), release TMEM to the next tile's MMAs,
 //               round to bf16 and store (TMA store of 128 x 64 boxes; masked
@@ -50,7 +51,7 @@ struct BsCfg {
   static constexpr int kBBytes = kBN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kGroup = 4;     // K blocks per scale word (one byte each)
-  static constexpr int kSfSlots = 4;   // groups of scale words in flight
+  static constexpr int kSfSlots = 6;   // groups of scale words in flight
   static constexpr int kSfaWords = kBM;
   static constexpr int kSfbWords = kBN;
   static constexpr int kSfSlotWords = kSfaWords + kSfbWords;
@@ -70,19 +71,24 @@ struct BsCfg {
 static_assert(BsCfg::kSfCol0 + BsCfg::kSfSlots * BsCfg::kSfSlotCols <= BsCfg::kTmemCols,
               "scale ring inside the TMEM allocation");
 static_assert(BsCfg::kSmemBytes <= 232448, "fits the opt-in shared memory of one CTA");
+static_assert((2 * BsCfg::kStages + 3 * BsCfg::kSfSlots + 3) * 8 + 8 <= BsCfg::kBarrierBytes,
+              "barriers, TMEM address and abort flag fit their area");
 
 // A positive normal power of two (exponent byte 1..255, no mantissa, no sign).
 __device__ __forceinline__ bool pow2_bits(uint32_t b) {
   return (b & 0x807FFFFFu) == 0 && (b >> 23) != 0;
 }
 
-template <bool MASKED>
+// SILU (masked only): the up projection with silu-and-mul and its quant in
+// the epilogue (interleaved gate/up weights; the output is q_out/q_scales).
+template <bool MASKED, bool SILU = false>
 __global__ void __launch_bounds__(BsCfg::kThreads, 1)
     gemm_block_fp8_bs(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   using C = BsCfg;
   constexpr int BN = C::kBN;
+  static_assert(!SILU || MASKED, "the fused silu-mul-quant output is a masked form");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
@@ -95,7 +101,8 @@ __global__ void __launch_bounds__(BsCfg::kThreads, 1)
   uint64_t* empty = full + C::kStages;
   uint64_t* sfull = empty + C::kStages;
   uint64_t* sempty = sfull + C::kSfSlots;
-  uint64_t* tfull = sempty + C::kSfSlots;
+  uint64_t* sload = sempty + C::kSfSlots;  // packed activation words landed in the slot
+  uint64_t* tfull = sload + C::kSfSlots;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
   uint32_t* tmem_slot = (uint32_t*)(drain + 1);
@@ -114,6 +121,7 @@ __global__ void __launch_bounds__(BsCfg::kThreads, 1)
     for (int s = 0; s < C::kSfSlots; ++s) {
       mbar_init(&sfull[s], 1);
       mbar_init(&sempty[s], 1);
+      mbar_init(&sload[s], 1);
     }
     mbar_init(tfull, 1);
     mbar_init(tempty, C::kEpiWarps);
@@ -227,107 +235,160 @@ __global__ void __launch_bounds__(BsCfg::kThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------------ scale loader ------------------------------
-    // Group q (tile q / gpt, K blocks 4 (q mod gpt) ..) is fetched into
-    // registers (all of its global loads issued together) several groups
-    // ahead of the one written to shared memory, the register sets rotating.
+    // Group q = tile q / gpt, K blocks 4 (q mod gpt) .. + 3.  Its global
+    // reads are started kAhead groups before it is written out.  Packed
+    // activation words come by one bulk copy into the group's slot (row r at
+    // word r) and are permuted in place when the group is written out; the
+    // weight scales (2 blocks x 4 K blocks: 16 contiguous bytes per block
+    // when K / 128 is a multiple of 4 and the array 16-byte aligned) by bulk
+    // copies into the slot's last 8 words, read before the slot's weight
+    // words are written.  Both wait for the slot to be free.  Otherwise
+    // (fp32 power-of-two activation scales; weight scales not so aligned)
+    // the values are loaded into registers.  Scale lines are pulled into L2
+    // kPrefetchGroups ahead.
+    constexpr int kAhead = 3;
+    constexpr int kPrefetchGroups = 8;
+    static_assert(kAhead < C::kSfSlots, "a copy lands in a slot the MMA has released");
     const int gpt = (KB + C::kGroup - 1) / C::kGroup;
     const int ngroups = my_tiles * gpt;
-    int cur_tt = -1, e = 0, m0 = 0, n0 = 0, ml = 0;
+    const bool packed = p.a_fmt == BFQ_SCALE_UE8M0_PACKED;
+    const bool wbulk = (KB & 3) == 0 && ((uintptr_t)p.sw & 15u) == 0;
+    const bool bulk = packed || wbulk;  // the group's slot receives bulk copies
+    const int nblks = (p.N + 127) / 128;
     bool bad = false;
-    struct Fetched {
-      uint32_t a[16];  // packed: a[c] = word of row 32 c + lane; pow2: a[4 c + k] = fp32 bits
-      uint32_t w;      // lane j < 8: fp32 bits of weight block nb0 + j / 4, K block i0 + j % 4
-      int nk;          // K blocks in this group
+    struct Coord {
+      int tt = -1, e = 0, m0 = 0, n0 = 0, ml = 0;
     };
-    auto fetch = [&](int q, Fetched& f) {
+    // first K block of group q; c holds its tile's coordinates (cached)
+    auto coord = [&](int q, Coord& c) -> int {
       const int tt = q / gpt;
-      const int i0 = (q - tt * gpt) * C::kGroup;
-      if (tt != cur_tt) {
-        cur_tt = tt;
-        persist_tile<MASKED>(blockIdx.x + tt * gridDim.x, p, tpre, cnt, e, m0, n0, ml);
+      if (tt != c.tt) {
+        c.tt = tt;
+        persist_tile<MASKED>(blockIdx.x + tt * gridDim.x, p, tpre, cnt, c.e, c.m0, c.n0, c.ml);
       }
-      const uint32_t* sa = (const uint32_t*)p.sa + (MASKED ? (int64_t)e * p.sa_estride : 0);
-      const float* sw = p.sw + (MASKED ? (int64_t)e * p.sw_estride : 0);
-      f.nk = min(C::kGroup, KB - i0);
+      return (q - tt * gpt) * C::kGroup;
+    };
+    auto sa_of = [&](const Coord& c) {
+      return (const uint32_t*)p.sa + (MASKED ? (int64_t)c.e * p.sa_estride : 0);
+    };
+    auto sw_of = [&](const Coord& c) {
+      return p.sw + (MASKED ? (int64_t)c.e * p.sw_estride : 0);
+    };
+    Coord c_pf, c_ld, c_em;
+    auto prefetch_group = [&](int q) {
+      const int i0 = coord(q, c_pf);
+      const int nk = min(C::kGroup, KB - i0);
+      const uint32_t* sa = sa_of(c_pf);
+      if (packed) {
+        // four 128-byte lines: rows 32 lane .. of the group's word column
+        if (lane < 4 && c_pf.m0 + 32 * lane < c_pf.ml)
+          prefetch_l2(sa + (int64_t)(i0 >> 2) * p.sa_ld + c_pf.m0 + 32 * lane);
+      } else if (lane < 16 && (lane >> 2) < nk && c_pf.m0 + 32 * (lane & 3) < c_pf.ml) {
+        prefetch_l2(sa + (int64_t)(i0 + (lane >> 2)) * p.sa_ld + c_pf.m0 + 32 * (lane & 3));
+      }
+      const int nb = c_pf.n0 / 128 + ((lane - 16) >> 2);
+      if (lane >= 16 && lane < 24 && nb < nblks && (lane & 3) < nk)
+        prefetch_l2(sw_of(c_pf) + (int64_t)nb * KB + i0 + (lane & 3));
+    };
+    struct Fetched {
+      uint32_t a[16];  // fp32 power-of-two scales: a[4 c + k] = bits of row 32 c + lane, K block k
+      uint32_t w;      // lane j < 8: fp32 bits of weight block n0 / 128 + j / 4, K block j % 4
+    };
+    int q_copied = 0;  // groups whose bulk copies were issued
+    auto fetch = [&](int q, Fetched& f) -> bool {
+      const int i0 = coord(q, c_ld);
+      const int nk = min(C::kGroup, KB - i0);
+      const uint32_t* sa = sa_of(c_ld);
+      const float* sw = sw_of(c_ld);
+      const int nb0 = c_ld.n0 / 128;
+      if (!wbulk) {
+        const int nb = nb0 + (lane >> 2), kb = i0 + (lane & 3);
+        f.w = (lane < 8 && nb < nblks && kb < KB) ? __float_as_uint(__ldg(sw + (int64_t)nb * KB + kb))
+                                                  : 0x3F800000u;
+      }
+      if (!packed) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int m = m0 + c * 32 + lane;
-        if (p.a_fmt == BFQ_SCALE_UE8M0_PACKED) {
-          f.a[c] = m < ml ? __ldg(sa + (int64_t)(i0 >> 2) * p.sa_ld + m) : 0u;
-        } else {
+        for (int c = 0; c < 4; ++c) {
+          const int m = c_ld.m0 + c * 32 + lane;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             f.a[4 * c + k] =
-                (m < ml && k < f.nk) ? __ldg(sa + (int64_t)(i0 + k) * p.sa_ld + m) : 0x3F800000u;
+                (m < c_ld.ml && k < nk) ? __ldg(sa + (int64_t)(i0 + k) * p.sa_ld + m) : 0x3F800000u;
         }
       }
-      const int nb = n0 / 128 + (lane >> 2), kb = i0 + (lane & 3);
-      f.w = (lane < 8 && nb < (p.N + 127) / 128 && kb < KB)
-                ? __float_as_uint(__ldg(sw + (int64_t)nb * KB + kb))
-                : 0x3F800000u;
-    };
-    // The scale lines of group q + kPrefetchGroups are pulled into L2 while
-    // group q is fetched: behind a full operand stream a scale line that
-    // missed L2 would otherwise cost an HBM round trip per group.
-    constexpr int kPrefetchGroups = 8;
-    int pf_tt = -1, pf_e = 0, pf_m0 = 0, pf_n0 = 0, pf_ml = 0;
-    auto prefetch_group = [&](int q) {
-      const int tt = q / gpt;
-      const int i0 = (q - tt * gpt) * C::kGroup;
-      if (tt != pf_tt) {
-        pf_tt = tt;
-        persist_tile<MASKED>(blockIdx.x + tt * gridDim.x, p, tpre, cnt, pf_e, pf_m0, pf_n0, pf_ml);
+      if (!bulk) return true;
+      const int slot = q % C::kSfSlots;
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&sempty[slot], ((uint32_t)(q / C::kSfSlots) & 1u) ^ 1u, abort_flag,
+                       p.status, kWaitTimeoutNs);
+        if (ok) {
+          uint32_t* wa = sf + slot * C::kSfSlotWords;
+          // rows m0 .. of the group's word column, not past the column's end
+          const uint32_t abytes = packed ? (uint32_t)min(kBM, (int)(p.sa_ld - c_ld.m0)) * 4u : 0u;
+          const int nbw = wbulk ? min(2, nblks - nb0) : 0;
+          mbar_arrive_expect_tx(&sload[slot], abytes + 16u * (uint32_t)nbw);
+          if (packed)
+            bulk_load_1d(wa, sa + (int64_t)(i0 >> 2) * p.sa_ld + c_ld.m0, abytes, &sload[slot]);
+          for (int h = 0; h < nbw; ++h)
+            bulk_load_1d(wa + C::kSfSlotWords - 8 + 4 * h, sw + (int64_t)(nb0 + h) * KB + i0, 16u,
+                         &sload[slot]);
+        }
       }
-      const uint32_t* sa = (const uint32_t*)p.sa + (MASKED ? (int64_t)pf_e * p.sa_estride : 0);
-      const float* sw = p.sw + (MASKED ? (int64_t)pf_e * p.sw_estride : 0);
-      const int nk = min(C::kGroup, KB - i0);
-      if (p.a_fmt == BFQ_SCALE_UE8M0_PACKED) {
-        // four 128-byte lines: rows 32 lane .. of the group's word column
-        if (lane < 4 && pf_m0 + 32 * lane < pf_ml)
-          prefetch_l2(sa + (int64_t)(i0 >> 2) * p.sa_ld + pf_m0 + 32 * lane);
-      } else if (lane < 16 && (lane >> 2) < nk && pf_m0 + 32 * (lane & 3) < pf_ml) {
-        prefetch_l2(sa + (int64_t)(i0 + (lane >> 2)) * p.sa_ld + pf_m0 + 32 * (lane & 3));
-      }
-      const int nb = pf_n0 / 128 + ((lane - 16) >> 2), kb = i0 + (lane & 3);
-      if (lane >= 16 && lane < 24 && nb < (p.N + 127) / 128 && (lane & 3) < nk)
-        prefetch_l2(sw + (int64_t)nb * KB + kb);
+      ok = __shfl_sync(0xFFFFFFFFu, (int)ok, 0) != 0;
+      if (ok) q_copied = q + 1;
+      return ok;
     };
     auto emit = [&](int q, const Fetched& f) -> bool {
+      const int i0 = coord(q, c_em);
+      const int nk = min(C::kGroup, KB - i0);
       const int slot = q % C::kSfSlots;
+      const uint32_t ph = (uint32_t)(q / C::kSfSlots) & 1u;
       // lane 0 waits and the warp takes its decision together (the shuffles
       // below need every lane)
       bool ok = true;
       if (lane == 0)
-        ok = mbar_wait(&sempty[slot], ((uint32_t)(q / C::kSfSlots) & 1u) ^ 1u, abort_flag,
-                       p.status, kWaitTimeoutNs);
+        ok = bulk ? mbar_wait(&sload[slot], ph, abort_flag, p.status, kWaitTimeoutNs)
+                  : mbar_wait(&sempty[slot], ph ^ 1u, abort_flag, p.status, kWaitTimeoutNs);
       if (!__shfl_sync(0xFFFFFFFFu, (int)ok, 0)) return false;
       __syncwarp();
       uint32_t* wa = sf + slot * C::kSfSlotWords;
       uint32_t* wb = wa + C::kSfaWords;
-      // activation row 32 c + lane -> word 4 lane + c (the copy puts bytes
-      // 16 r + 4 c of the source at lane r, column c)
+      // activation row 32 c + lane -> word 4 lane + c (the copy into TMEM
+      // puts bytes 16 r + 4 c of the source at lane r, column c)
+      uint32_t v[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t w = f.a[c];
-        if (p.a_fmt != BFQ_SCALE_UE8M0_PACKED) {
-          w = 0;
+        const int m = c_em.m0 + c * 32 + lane;
+        if (packed) {
+          v[c] = m < c_em.ml ? wa[c * 32 + lane] : 0u;
+        } else {
+          v[c] = 0;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t b = f.a[4 * c + k];
             bad |= !pow2_bits(b);
-            w |= k < f.nk ? ((b >> 23) & 0xFFu) << (8 * k) : 0u;
+            v[c] |= k < nk ? ((b >> 23) & 0xFFu) << (8 * k) : 0u;
           }
         }
-        wa[lane * 4 + c] = w;
       }
+      // lane j < 8: fp32 bits of weight block n0 / 128 + j / 4, K block j % 4
+      // (a block past N keeps the value 1.0, unused)
+      uint32_t w = f.w;
+      if (wbulk)
+        w = (lane < 8 && c_em.n0 / 128 + (lane >> 2) < nblks) ? wb[C::kSfbWords - 8 + lane]
+                                                             : 0x3F800000u;
+      __syncwarp();  // every copied word is read before any is overwritten
+#pragma unroll
+      for (int c = 0; c < 4; ++c) wa[lane * 4 + c] = v[c];
       // weight rows: one word per 128-row block, the same for all its rows
-      if (lane < 8) bad |= !pow2_bits(f.w);
+      if (lane < 8) bad |= !pow2_bits(w);
       uint32_t wv0 = 0, wv1 = 0;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, f.w, k);
-        const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, f.w, 4 + k);
-        if (k < f.nk) {
+        const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, w, k);
+        const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, w, 4 + k);
+        if (k < nk) {
           wv0 |= ((b0 >> 23) & 0xFFu) << (8 * k);
           wv1 |= ((b1 >> 23) & 0xFFu) << (8 * k);
         }
@@ -339,23 +400,33 @@ __global__ void __launch_bounds__(BsCfg::kThreads, 1)
       if (lane == 0) mbar_arrive(&sfull[slot]);
       return true;
     };
-    // kFetchAhead groups' loads in flight while one is written (under a
-    // full operand stream an L2 hit takes ~2 us, four K blocks of MMA less)
-    constexpr int kFetchAhead = 3;
-    Fetched f[kFetchAhead + 1];
+    Fetched f[kAhead + 1];
+    bool stop = false;
+    int q_emitted = 0;
     for (int q = 0; q < kPrefetchGroups && q < ngroups; ++q) prefetch_group(q);
 #pragma unroll
-    for (int d = 0; d < kFetchAhead; ++d)
-      if (d < ngroups) fetch(d, f[d]);
-    bool stop = false;
-    for (int q0 = 0; q0 < ngroups && !stop; q0 += kFetchAhead + 1) {
+    for (int d = 0; d < kAhead; ++d)
+      if (!stop && d < ngroups) stop = !fetch(d, f[d]);
+    for (int q0 = 0; q0 < ngroups && !stop; q0 += kAhead + 1) {
 #pragma unroll
-      for (int d = 0; d <= kFetchAhead; ++d) {
+      for (int d = 0; d <= kAhead; ++d) {
         const int q = q0 + d;
         if (stop || q >= ngroups) continue;
         if (q + kPrefetchGroups < ngroups) prefetch_group(q + kPrefetchGroups);
-        if (q + kFetchAhead < ngroups) fetch(q + kFetchAhead, f[(d + kFetchAhead) % (kFetchAhead + 1)]);
-        stop = !emit(q, f[d]);
+        if (q + kAhead < ngroups)
+          stop = !fetch(q + kAhead, f[(d + kAhead) % (kAhead + 1)]);
+        if (!stop) {
+          stop = !emit(q, f[d]);
+          if (!stop) q_emitted = q + 1;
+        }
+      }
+    }
+    if (stop && lane == 0) {
+      // let the bulk copies already issued land before the CTA can exit
+      for (int q = q_emitted; q < q_copied; ++q) {
+        volatile int no_abort = 0;
+        (void)mbar_wait(&sload[q % C::kSfSlots], (uint32_t)(q / C::kSfSlots) & 1u, &no_abort,
+                        p.status, kWaitTimeoutNs / 8);
       }
     }
     if (bad) atomicCAS(p.status, 0, BFQ_ERR_FORMAT);
@@ -371,24 +442,30 @@ __global__ void __launch_bounds__(BsCfg::kThreads, 1)
       int e, m0, n0, m_limit;
       persist_tile<MASKED>(blockIdx.x + tt * gridDim.x, p, tpre, cnt, e, m0, n0, m_limit);
       const int col0 = n0 + half * 128;
-      const bool warp_active = (m0 + quarter * 32 < m_limit) && col0 < p.N;
+      const bool warp_active = (m0 + quarter * 32 < m_limit) && (SILU || col0 < p.N);
       const int ncols = min(128, p.N - col0);
-      uint64_t lo[32], hi[32];
+      uint64_t lo[32], hi[32];  // SILU: lo = 64 gate columns, hi = the matching up columns
       const bool stop = !mbar_wait(tfull, (uint32_t)tt & 1u, abort_flag, p.status,
                                    kWaitTimeoutNs);
       if (!stop) {
         tc_fence_after_sync();
         if (warp_active) {
-          const uint32_t taddr =
-              tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * 128);
+          const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                 (uint32_t)(half * (SILU ? 64 : 128));
           tmem_ld64_pairs_wait(taddr, lo);
-          tmem_ld64_pairs_wait(taddr + 64u, hi);
+          tmem_ld64_pairs_wait(taddr + (SILU ? 128u : 64u), hi);
         }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty);  // the next tile's MMAs may start
       }
       if (named_barrier_or(2, C::kEpiWarps * 32, stop || *abort_flag)) break;
+      if constexpr (SILU) {
+        silu_quant_tile_rows<C::kEpiWarps * 32>(p, lo, hi, (float*)stg, e, m0 + row_local, n0,
+                                                half, row_local,
+                                                warp_active && m0 + row_local < m_limit);
+        continue;
+      }
 
       // Box b (columns 64 b .. 64 b + 63 of the tile) is held by warp half
       // b / 2 (lo or hi); staged as bf16 in the 128-byte swizzled layout:
@@ -447,13 +524,14 @@ __global__ void __launch_bounds__(BsCfg::kThreads, 1)
 // ----------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------
-template <bool MASKED>
+template <bool MASKED, bool SILU = false>
 bfq_status configure_bs(const DeviceInfo& dev) {
   static bool configured[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (configured[dev.ordinal]) return BFQ_OK;
-  if (cudaFuncSetAttribute(gemm_block_fp8_bs<MASKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm_block_fp8_bs<MASKED, SILU>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)BsCfg::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     return BFQ_ERR_CUDA;
@@ -473,14 +551,14 @@ bool pow2_fmt(int32_t fmt) {
   return fmt == BFQ_SCALE_UE8M0_PACKED || fmt == BFQ_SCALE_F32_POW2;
 }
 
-template <bool MASKED>
+template <bool MASKED, bool SILU = false>
 bfq_status launch_bs(const DeviceInfo& dev, const CUtensorMap& ma, const CUtensorMap& mw,
                      const CUtensorMap& mo, const GemmParams& p, int64_t tiles,
                      cudaStream_t s) {
-  bfq_status st = configure_bs<MASKED>(dev);
+  bfq_status st = configure_bs<MASKED, SILU>(dev);
   if (st != BFQ_OK) return st;
   const unsigned grid = (unsigned)(tiles < dev.sm_count ? tiles : dev.sm_count);
-  return launch_status(launch_pdl(gemm_block_fp8_bs<MASKED>, dim3(grid),
+  return launch_status(launch_pdl(gemm_block_fp8_bs<MASKED, SILU>, dim3(grid),
                                   dim3(BsCfg::kThreads), BsCfg::kSmemBytes, s, 1u, ma, mw, mo,
                                   p));
 }
@@ -503,7 +581,8 @@ extern "C" bfq_status bfq_gemm_block_fp8_ue8m0(const void* a_q, const void* a_sc
   if (M == 0) return BFQ_OK;
   if (!a_q || !a_scales || !w_q || !w_scales || !out) return BFQ_ERR_INVALID_ARG;
   if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(out) || a_scale_ld % 4 != 0 ||
-      ((uintptr_t)a_scales & 3u) || ((uintptr_t)w_scales & 3u))
+      ((uintptr_t)a_scales & 3u) || ((uintptr_t)w_scales & 3u) ||
+      (a_fmt == BFQ_SCALE_UE8M0_PACKED && !aligned16(a_scales)))
     return BFQ_ERR_MISALIGNED;
   DeviceInfo dev;
   bfq_status st = check_device_bs(&dev);
@@ -554,7 +633,8 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked_ue8m0(
   if (!a_q || !a_scales || !w_q || !w_scales || !valid_counts || !out)
     return BFQ_ERR_INVALID_ARG;
   if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(out) || a_scale_ld % 4 != 0 ||
-      ((uintptr_t)a_scales & 3u) || ((uintptr_t)w_scales & 3u))
+      ((uintptr_t)a_scales & 3u) || ((uintptr_t)w_scales & 3u) ||
+      (a_fmt == BFQ_SCALE_UE8M0_PACKED && !aligned16(a_scales)))
     return BFQ_ERR_MISALIGNED;
   DeviceInfo dev;
   bfq_status st = check_device_bs(&dev);
@@ -584,4 +664,58 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked_ue8m0(
   p.E = E;
   return launch_bs<true>(dev, ma, mw, mw, p, (int64_t)p.m_tiles * p.n_tiles * E,
                          (cudaStream_t)stream);
+}
+
+extern "C" bfq_status bfq_gemm_block_fp8_masked_silu_quant_ue8m0(
+    const void* a_q, const void* a_scales, int32_t a_fmt, int64_t a_scale_ld, const void* w_q,
+    const float* w_scales, const int32_t* valid_counts, int32_t E, int32_t T, int64_t I,
+    int64_t K, int32_t q_fmt, void* q_out, void* q_scales, int64_t q_scale_ld, void* stream) {
+  if (E < 0 || T < 0 || I <= 0 || K <= 0 || !valid_fmt(a_fmt) || !valid_fmt(q_fmt) ||
+      a_scale_ld < T || q_scale_ld < T)
+    return BFQ_ERR_INVALID_ARG;
+  if (!pow2_fmt(a_fmt)) return BFQ_ERR_FORMAT;
+  if (K % 128 != 0 || I % 128 != 0) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  const int64_t N = 2 * I;
+  if ((int64_t)E * T > 0x7FFFFFFF || (int64_t)E * N > 0x7FFFFFFF || K > 0x7FFFFFFF ||
+      (int64_t)T * I > 0x7FFFFFFF)
+    return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (E > kPersistMaxExperts) return BFQ_ERR_UNSUPPORTED_SHAPE;
+  if (E == 0 || T == 0) return BFQ_OK;
+  if (!a_q || !a_scales || !w_q || !w_scales || !valid_counts || !q_out || !q_scales)
+    return BFQ_ERR_INVALID_ARG;
+  if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(q_out) || a_scale_ld % 4 != 0 ||
+      q_scale_ld % 4 != 0 || ((uintptr_t)a_scales & 3u) || ((uintptr_t)w_scales & 3u) ||
+      ((uintptr_t)q_scales & 3u) || (a_fmt == BFQ_SCALE_UE8M0_PACKED && !aligned16(a_scales)))
+    return BFQ_ERR_MISALIGNED;
+  DeviceInfo dev;
+  bfq_status st = check_device_bs(&dev);
+  if (st != BFQ_OK) return st;
+  CUtensorMap ma, mw;
+  if (!make_map(&ma, a_q, (uint64_t)K, (uint64_t)E * T, kBM) ||
+      !make_map(&mw, w_q, (uint64_t)K, (uint64_t)E * N, (uint32_t)BsCfg::kBN))
+    return BFQ_ERR_CUDA;
+  GemmParams p{};
+  p.sa = a_scales;
+  p.sa_ld = a_scale_ld;
+  p.sa_estride = scale_cols(K, a_fmt) * a_scale_ld;
+  p.sw = w_scales;
+  p.sw_estride = (N / 128) * (K / 128);
+  p.counts = valid_counts;
+  p.status = device_status_ptr();
+  if (!p.status) return BFQ_ERR_CUDA;
+  p.M = T;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.m_tiles = (int)cdiv(T, kBM);
+  p.n_tiles = (int)(N / BsCfg::kBN);
+  p.splits = 1;
+  p.a_fmt = a_fmt;
+  p.E = E;
+  p.q_out = (uint8_t*)q_out;
+  p.q_scales = q_scales;
+  p.q_scale_ld = q_scale_ld;
+  p.q_fmt = q_fmt;
+  p.silu_tab = silu_table(dev, (cudaStream_t)stream);
+  return launch_bs<true, true>(dev, ma, mw, mw, p, (int64_t)p.m_tiles * p.n_tiles * E,
+                               (cudaStream_t)stream);
 }

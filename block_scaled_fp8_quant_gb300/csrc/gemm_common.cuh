@@ -113,4 +113,81 @@ __device__ __forceinline__ void masked_tile_prefix(const GemmParams& p, int* tpr
   }
 }
 
+// Fused silu(gate) * up + 1 x 128 group quant of one output tile's features,
+// exactly as the silu-mul-quant kernel computes them from the bf16
+// up-projection output ("[EP+DP] Optimize the little operations in the
+// DeepGEMM + DeepEP low latency case", Summary item 2): a 256-wide tile of
+// the interleaved up projection holds gate block n0 / 256 (columns 0-127)
+// and the matching up block (128-255).  Each thread holds, for its row, the
+// fp32 accumulators of 64 gate features g[] and the same 64 up features u[]
+// (features 64 half .. + 63, as 32 pairs each).  Gate and up are rounded to
+// bf16, y = silu(g) * u in fp32 (silu looked up in the library's table of
+// all bf16 gates, or computed while a graph is captured before the table
+// exists — the same values), group amax over the 128 features (the two
+// halves exchanged through xam, shared float[2][128]), scale, codes.  y
+// overwrites g.  Called by all kNT epilogue threads (named barrier 1);
+// active = the row is valid and the thread's warp holds data.
+template <int kNT>
+__device__ __forceinline__ void silu_quant_tile_rows(const GemmParams& p, uint64_t* g,
+                                                     const uint64_t* u, float* xam, int e, int m,
+                                                     int n0, int half, int row_local,
+                                                     bool active) {
+  float amax = 0.0f;
+  if (active) {  // rows past the count: nothing to form
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float2 gf = unpack2(g[j]), uf = unpack2(u[j]);
+      const uint32_t gb = pack_bf16x2(gf.x, gf.y), ub = pack_bf16x2(uf.x, uf.y);
+      const float2 sg = p.silu_tab ? make_float2(__ldg(p.silu_tab + (gb & 0xFFFFu)),
+                                                 __ldg(p.silu_tab + (gb >> 16)))
+                                   : bfq_silu2(bf16lo(gb), bf16hi(gb));
+      const float2 y = unpack2(mul2_rn(pack2(sg.x, sg.y), pack2(bf16lo(ub), bf16hi(ub))));
+      g[j] = pack2(y.x, y.y);
+      amax = fmaxf(amax, fmaxf(fabsf(y.x), fabsf(y.y)));
+    }
+  }
+  xam[half * kBM + row_local] = amax;  // partial amax per half and row
+  named_barrier(1, kNT);
+  amax = fmaxf(xam[row_local], xam[kBM + row_local]);
+  named_barrier(1, kNT);  // both read before the next tile writes
+  if (!active) return;
+  const int I = p.N >> 1;
+  const int fg = n0 >> 8;  // 128-feature group of this tile
+  float sc = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
+  if (p.q_fmt != BFQ_SCALE_F32) sc = ceil_pow2(sc);
+  const float y_inv = __frcp_rn(sc);
+  uint8_t* qrow = p.q_out + ((int64_t)e * p.M + m) * I + fg * 128 + half * 64;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {  // 16 codes per 16-byte store
+    uint32_t w[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 y0 = unpack2(g[c * 8 + 2 * t]), y1 = unpack2(g[c * 8 + 2 * t + 1]);
+      uint32_t lo, hi;
+      if (p.q_fmt == BFQ_SCALE_F32) {
+        lo = cvt_e4m3x2(group_div(y0.x, sc, y_inv), group_div(y0.y, sc, y_inv));
+        hi = cvt_e4m3x2(group_div(y1.x, sc, y_inv), group_div(y1.y, sc, y_inv));
+      } else {
+        lo = cvt_e4m3x2(__fmul_rn(y0.x, y_inv), __fmul_rn(y0.y, y_inv));
+        hi = cvt_e4m3x2(__fmul_rn(y1.x, y_inv), __fmul_rn(y1.y, y_inv));
+      }
+      w[t] = lo | (hi << 16);
+    }
+    st_v4(qrow + c * 16, make_uint4(w[0], w[1], w[2], w[3]));
+  }
+  if (half == 0) {
+    const int G = I >> 7;
+    if (p.q_fmt == BFQ_SCALE_UE8M0_PACKED) {
+      const int64_t cols = (G + 3) >> 2;
+      uint8_t* word =
+          (uint8_t*)p.q_scales + (((int64_t)e * cols + (fg >> 2)) * p.q_scale_ld + m) * 4;
+      word[fg & 3] = (uint8_t)ue8m0_byte(sc);
+      if (fg == G - 1)
+        for (int b = (fg & 3) + 1; b < 4; ++b) word[b] = 0;
+    } else {
+      ((float*)p.q_scales)[((int64_t)e * G + fg) * p.q_scale_ld + m] = sc;
+    }
+  }
+}
+
 }  // namespace bfq

@@ -859,74 +859,8 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
       if (named_barrier_or(2, C::kEpiWarps * 32, stop || *abort_flag)) break;
 
       if constexpr (SILU) {
-        // Fused silu(gate) * up + 1 x 128 group quant of the features of this
-        // tile, exactly as the silu-mul-quant kernel computes them from the
-        // bf16 up-projection output (silu looked up in the library's table of
-        // all bf16 gates, or computed while a graph is captured before the
-        // table exists — the same values) ("[EP+DP] Optimize the little operations
-        // in the DeepGEMM + DeepEP low latency case", Summary item 2): gate
-        // and up rounded to bf16, y = silu(g) * u in fp32, group amax over the
-        // 128 features (this thread's 64 and the other half-warp's 64,
-        // exchanged through shared memory), scale, codes.
-        float amax = 0.0f;
-        if (warp_active && row_ok) {  // rows past the count: nothing to form
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float2 gf = unpack2(acc[j]), uf = unpack2(acc[32 + j]);
-            const uint32_t gb = pack_bf16x2(gf.x, gf.y), ub = pack_bf16x2(uf.x, uf.y);
-            const float2 sg = p.silu_tab
-                                  ? make_float2(__ldg(p.silu_tab + (gb & 0xFFFFu)),
-                                                __ldg(p.silu_tab + (gb >> 16)))
-                                  : bfq_silu2(bf16lo(gb), bf16hi(gb));
-            const float2 y = unpack2(mul2_rn(pack2(sg.x, sg.y), pack2(bf16lo(ub), bf16hi(ub))));
-            acc[j] = pack2(y.x, y.y);
-            amax = fmaxf(amax, fmaxf(fabsf(y.x), fabsf(y.y)));
-          }
-        }
-        float* xam = (float*)stg;  // [2][128] partial amax per half and row
-        xam[half * kBM + row_local] = amax;
-        named_barrier(1, C::kEpiWarps * 32);
-        amax = fmaxf(xam[row_local], xam[kBM + row_local]);
-        named_barrier(1, C::kEpiWarps * 32);  // both read before the next tile writes
-        if (warp_active && row_ok) {
-          const int I = p.N >> 1;
-          const int fg = n0 >> 8;  // 128-feature group of this tile
-          float sc = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
-          if (p.q_fmt != BFQ_SCALE_F32) sc = ceil_pow2(sc);
-          const float y_inv = __frcp_rn(sc);
-          uint8_t* qrow = p.q_out + ((int64_t)e * p.M + m) * I + fg * 128 + half * 64;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {  // 16 codes per 16-byte store
-            uint32_t w[4];
-#pragma unroll
-            for (int t2 = 0; t2 < 4; ++t2) {
-              const float2 y0 = unpack2(acc[c * 8 + 2 * t2]), y1 = unpack2(acc[c * 8 + 2 * t2 + 1]);
-              uint32_t lo, hi;
-              if (p.q_fmt == BFQ_SCALE_F32) {
-                lo = cvt_e4m3x2(group_div(y0.x, sc, y_inv), group_div(y0.y, sc, y_inv));
-                hi = cvt_e4m3x2(group_div(y1.x, sc, y_inv), group_div(y1.y, sc, y_inv));
-              } else {
-                lo = cvt_e4m3x2(__fmul_rn(y0.x, y_inv), __fmul_rn(y0.y, y_inv));
-                hi = cvt_e4m3x2(__fmul_rn(y1.x, y_inv), __fmul_rn(y1.y, y_inv));
-              }
-              w[t2] = lo | (hi << 16);
-            }
-            st_v4(qrow + c * 16, make_uint4(w[0], w[1], w[2], w[3]));
-          }
-          if (half == 0) {
-            const int G = I >> 7;
-            if (p.q_fmt == BFQ_SCALE_UE8M0_PACKED) {
-              const int64_t cols = (G + 3) >> 2;
-              uint8_t* word = (uint8_t*)p.q_scales +
-                              (((int64_t)e * cols + (fg >> 2)) * p.q_scale_ld + m) * 4;
-              word[fg & 3] = (uint8_t)ue8m0_byte(sc);
-              if (fg == G - 1)
-                for (int bb = (fg & 3) + 1; bb < 4; ++bb) word[bb] = 0;
-            } else {
-              ((float*)p.q_scales)[((int64_t)e * G + fg) * p.q_scale_ld + m] = sc;
-            }
-          }
-        }
+        silu_quant_tile_rows<C::kEpiWarps * 32>(p, acc, acc + 32, (float*)stg, e, m, n0, half,
+                                                row_local, warp_active && row_ok);
       } else if (MASKED) {
         // Rows past the count must not be written, so no TMA store: each
         // 128 x 64 box is staged in shared memory (128-byte swizzle, as for

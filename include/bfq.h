@@ -325,7 +325,8 @@ bfq_status bfq_gemm_block_fp8_masked(const void* a_q, const void* a_scales, int3
  *
  *   a_q, a_scale_ld, w_q, M, N, K, out   as for bfq_gemm_block_fp8.
  *   a_fmt          BFQ_SCALE_UE8M0_PACKED or BFQ_SCALE_F32_POW2 (else FORMAT).
- *   a_scales       column-major, as for bfq_gemm_block_fp8.
+ *   a_scales       column-major, as for bfq_gemm_block_fp8; packed UE8M0
+ *                  words 16-byte aligned (they are moved by bulk copies).
  *   w_scales       float [ceil(N/128)][K/128], each a positive power of two
  *                  2^-126 .. 2^127 (as bfq_weight_block_quant writes them with
  *                  fmt = BFQ_SCALE_F32_POW2).
@@ -402,6 +403,24 @@ bfq_status bfq_gemm_block_fp8_masked_silu_quant(const void* a_q, const void* a_s
                                                 int32_t T, int64_t I, int64_t K, int32_t q_fmt,
                                                 void* q_out, void* q_scales, int64_t q_scale_ld,
                                                 void* stream);
+
+/*
+ * bfq_gemm_block_fp8_masked_silu_quant on the block-scaled kernel of
+ * bfq_gemm_block_fp8_masked_ue8m0 (power-of-two scales on both operands,
+ * applied by the MMA): q_out and q_scales equal, bit for bit,
+ * bfq_silu_mul_quant of the bf16 output of bfq_gemm_block_fp8_masked_ue8m0
+ * with the un-interleaved weight.  Arguments as for
+ * bfq_gemm_block_fp8_masked_silu_quant; a_fmt BFQ_SCALE_UE8M0_PACKED or
+ * BFQ_SCALE_F32_POW2 (else FORMAT); w_scales powers of two (a scale that is
+ * not latches BFQ_ERR_FORMAT in the device status, as for
+ * bfq_gemm_block_fp8_ue8m0).
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE (also E > 1024), MISALIGNED, FORMAT,
+ * CUDA, DEVICE.
+ */
+bfq_status bfq_gemm_block_fp8_masked_silu_quant_ue8m0(
+    const void* a_q, const void* a_scales, int32_t a_fmt, int64_t a_scale_ld, const void* w_q,
+    const float* w_scales, const int32_t* valid_counts, int32_t E, int32_t T, int64_t I,
+    int64_t K, int32_t q_fmt, void* q_out, void* q_scales, int64_t q_scale_ld, void* stream);
 
 /*
  * Process-wide switch for programmatic dependent launch ([DG-bench] §4.2: the

@@ -179,6 +179,35 @@ def test_ue8m0_rejects_non_pow2_formats(cuda_lib, orc):
     _check_dense(orc, out, aq, sa, wq, sw, 2, "after a rejected call", rows=_sample_rows(M, 5))
 
 
+def test_ue8m0_weight_scales_loaded_either_way(cuda_lib, orc):
+    """Weight scales 16-byte aligned with K / 128 a multiple of 4 move by bulk
+    copies; at a 4-byte offset the kernel loads them into registers: the
+    two give the same output bit for bit.  Packed activation scales off a
+    16-byte boundary are refused."""
+    bfq = cuda_lib
+    M, N, K = 512, 9728, 2048
+    assert _on_block_scaled_plan(M, N, K)
+    aq, sa, wq, sw, d = _dense_problem(orc, M, N, K, 2, seed=77)
+    a_out = bfq.gemm_ue8m0(d[0], d[1], 2, d[2], d[3])
+    buf = torch.empty(d[3].numel() + 1, dtype=torch.float32, device="cuda")
+    sw_off = buf[1:].view_as(d[3])
+    sw_off.copy_(d[3])
+    assert sw_off.data_ptr() % 16 == 4
+    b_out = torch.empty_like(a_out)
+    bfq.bfq_gemm_block_fp8_ue8m0(d[0], d[1], 2, d[1].shape[-1], d[2], sw_off, b_out)
+    torch.cuda.synchronize()
+    assert bfq.bfq_poll_device_status() == 0
+    assert torch.equal(a_out, b_out)
+    _check_dense(orc, b_out, aq, sa, wq, sw, 2, "register-loaded weight scales",
+                 rows=_sample_rows(M, 77))
+    sbuf = torch.empty(d[1].numel() + 1, dtype=torch.int32, device="cuda")
+    sa_off = sbuf[1:].view_as(d[1])
+    sa_off.copy_(d[1])
+    with pytest.raises(bfq.BfqError) as ei:
+        bfq.bfq_gemm_block_fp8_ue8m0(d[0], sa_off, 2, d[1].shape[-1], d[2], d[3], b_out)
+    assert ei.value.status == 3  # BFQ_ERR_MISALIGNED
+
+
 def _expert_problem(orc, E, T, N, K, counts, seed, experts=None):
     """Per-expert operands with packed UE8M0 activation scales and
     power-of-two weight scales; padded activation rows hold the e4m3 NaN
@@ -311,3 +340,103 @@ def test_ue8m0_full_size_sampled(cuda_lib, orc, N, K):
     got = out.float().cpu().numpy()[rows]
     assert_gemm_close(got, ref, an, wn, f"ue8m0 m={M} n={N} k={K}")
     assert calc_diff(got, ref) < 1e-4
+
+
+SENT = 0x3C3C3C3C
+
+
+@pytest.mark.parametrize("q_fmt", [0, 1, 2])
+@pytest.mark.parametrize("E,T,H,I,counts", [
+    (3, 136, 512, 256, [70, 0, 136]),
+    (4, 256, 1152, 384, [1, 128, 129, 256]),   # 9 K blocks; a packed word left partial
+])
+def test_ue8m0_fused_silu_quant_equals_unfused_chain(cuda_lib, orc, q_fmt, E, T, H, I, counts):
+    """The up projection with silu-mul-quant in the block-scaled kernel's
+    epilogue equals, bit for bit, the block-scaled masked GEMM to bf16
+    followed by the silu-mul-quant kernel, and the oracle's silu-mul-quant of
+    that bf16 output; padded rows and scale columns are never written."""
+    bfq = cuda_lib
+    cnt = np.array(counts, np.int32)
+    d_cnt = torch.from_numpy(cnt).cuda()
+    x = synth.masked_activation(E, T, H, torch.from_numpy(cnt), seed=E * 100 + I + 7,
+                                poison=False)
+    a = torch.zeros((E, T, H), dtype=torch.float8_e4m3fn, device="cuda")
+    sa = torch.zeros((E, bfq.scale_cols(H, 2), T), dtype=torch.int32, device="cuda")
+    for e in range(E):
+        if cnt[e]:
+            bfq.bfq_quant(_spread(x[e, :cnt[e]]).cuda(), a[e, :cnt[e]], sa[e], 2, T)
+    w = synth.expert_weights(E, 2 * I, H, seed=E * 100 + I + 8)
+    wq, sw = bfq.weight_block_quant(w.cuda(), 1)
+    h = torch.full((E, T, 2 * I), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bfq.gemm_masked_ue8m0(a, sa, 2, wq, sw, d_cnt, out=h)
+    q_u, sc_u = bfq.silu_mul_quant(h, d_cnt, q_fmt)
+    wq_i, sw_i = bfq.interleave_gate_up(wq, sw)
+    q_f = torch.full((E, T, I), 0x7E, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    sc_f = torch.full((E, bfq.scale_cols(I, q_fmt), T), SENT, dtype=torch.int32, device="cuda")
+    bfq.bfq_gemm_block_fp8_masked_silu_quant_ue8m0(a, sa, 2, T, wq_i, sw_i, d_cnt, q_fmt, q_f,
+                                                   sc_f, T)
+    torch.cuda.synchronize()
+    assert bfq.bfq_poll_device_status() == 0
+    qf, qu = codes(q_f), codes(q_u)
+    sf, su = scale_np(sc_f, q_fmt), scale_np(sc_u, q_fmt)
+    sent = np.array([SENT], np.uint32).view(np.float32 if q_fmt != 2 else np.uint32)[0]
+    for e in range(E):
+        c = int(cnt[e])
+        assert np.array_equal(qf[e, :c], qu[e, :c]), f"expert {e}: codes"
+        assert np.array_equal(sf[e][:, :c], su[e][:, :c]), f"expert {e}: scales"
+        assert (qf[e, c:] == 0x7E).all(), f"expert {e}: padded rows written"
+        assert np.array_equal(sf[e][:, c:], np.full_like(sf[e][:, c:], sent)), \
+            f"expert {e}: padded scale columns written"
+        if c:
+            oq, osc = orc.silu_mul_quant(bits(h[e:e + 1, :c]), np.array([c], np.int32), q_fmt,
+                                         scale_ld=T)
+            assert np.array_equal(qf[e, :c], oq[0]), f"expert {e}: codes vs oracle"
+            assert np.array_equal(sf[e][:, :c], osc[0][:, :c]), f"expert {e}: scales vs oracle"
+
+
+@pytest.mark.slow
+def test_ue8m0_fused_silu_quant_moe_config(cuda_lib, orc):
+    """The MoE configuration (E=32, T=256, H=7168, I=2048, counts ~U{0..256},
+    packed UE8M0): fused equals the unfused block-scaled chain on every valid
+    row; on three experts the fused codes and scales equal the oracle's
+    silu-mul-quant of the GPU's bf16 up output."""
+    bfq = cuda_lib
+    E, T, H, I = 32, 256, 7168, 2048
+    counts = synth.valid_counts(E, T)
+    d_cnt = counts.cuda()
+    x = synth.masked_activation(E, T, H, counts, seed=901, device="cuda", poison=False)
+    a = torch.zeros((E, T, H), dtype=torch.float8_e4m3fn, device="cuda")
+    sa = torch.zeros((E, bfq.scale_cols(H, 2), T), dtype=torch.int32, device="cuda")
+    for e in range(E):
+        c = int(counts[e])
+        if c:
+            bfq.bfq_quant(x[e, :c], a[e, :c], sa[e], 2, T)
+    del x
+    wq = torch.empty((E, 2 * I, H), dtype=torch.float8_e4m3fn, device="cuda")
+    sw = torch.empty((E, 2 * I // 128, H // 128), dtype=torch.float32, device="cuda")
+    for e in range(E):
+        q1, s1 = bfq.weight_block_quant(synth.weight(2 * I, H, seed=700 + e, device="cuda"), 1)
+        wq[e].copy_(q1)
+        sw[e].copy_(s1)
+    h = bfq.gemm_masked_ue8m0(a, sa, 2, wq, sw, d_cnt)
+    q_u, sc_u = bfq.silu_mul_quant(h, d_cnt, 2)
+    wq_i, sw_i = bfq.interleave_gate_up(wq, sw)
+    del wq, sw
+    q_f = torch.empty((E, T, I), dtype=torch.float8_e4m3fn, device="cuda")
+    sc_f = torch.empty((E, bfq.scale_cols(I, 2), T), dtype=torch.int32, device="cuda")
+    bfq.bfq_gemm_block_fp8_masked_silu_quant_ue8m0(a, sa, 2, T, wq_i, sw_i, d_cnt, 2, q_f, sc_f,
+                                                   T)
+    torch.cuda.synchronize()
+    assert bfq.bfq_poll_device_status() == 0
+    qf, qu = codes(q_f), codes(q_u)
+    sf, su = scale_np(sc_f, 2), scale_np(sc_u, 2)
+    live = [e for e in range(E) if int(counts[e]) > 0]
+    for e in range(E):
+        c = int(counts[e])
+        assert np.array_equal(qf[e, :c], qu[e, :c]), f"expert {e}"
+        assert np.array_equal(sf[e][:, :c], su[e][:, :c]), f"expert {e}"
+    for e in sorted({live[0], live[len(live) // 2], live[-1]}):
+        c = int(counts[e])
+        oq, osc = orc.silu_mul_quant(bits(h[e:e + 1, :c]), np.array([c], np.int32), 2,
+                                     scale_ld=T)
+        assert np.array_equal(qf[e, :c], oq[0]) and np.array_equal(sf[e][:, :c], osc[0][:, :c])
