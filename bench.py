@@ -96,6 +96,7 @@ def kernel_source_hash():
 
     h = hashlib.sha256()
     for rel in ("block_scaled_fp8_quant_gb300/csrc/gemm_kernels.cu",
+                "block_scaled_fp8_quant_gb300/csrc/gemm_common.cuh",
                 "block_scaled_fp8_quant_gb300/csrc/bfq_device.cuh",
                 "block_scaled_fp8_quant_gb300/csrc/quant_kernels.cu"):
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
@@ -354,6 +355,29 @@ def build_problem(bfq, torch, dev, only=None):
                                out=out, ws=ws))
     torch.cuda.synchronize()
     return shapes
+
+
+def profile_ue8m0_shape(bfq, torch, dev, shape, calls):
+    """One (m, n, k) with UE8M0 scales on both operands (packed activation
+    scales, power-of-two weight scales), `calls` eager rounds of quant +
+    bfq_gemm_block_fp8_ue8m0, for profiler captures."""
+    import bfq_synth as synth
+
+    m, n, k = shape
+    w = synth.weight(n, k, seed=n + k, device=dev)
+    wq, sw = bfq.weight_block_quant(w, bfq.SCALE_F32_POW2)
+    del w
+    x = synth.activation(m, k, seed=m * 31 + n, device=dev)
+    q = torch.empty((m, k), dtype=torch.float8_e4m3fn, device=dev)
+    s = torch.empty((bfq.scale_cols(k, bfq.SCALE_UE8M0_PACKED), bfq.align4(m)), dtype=torch.int32,
+                    device=dev)
+    out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    for _ in range(calls):
+        bfq.bfq_quant(x, q, s, bfq.SCALE_UE8M0_PACKED, s.shape[-1])
+        bfq.bfq_gemm_block_fp8_ue8m0(q, s, bfq.SCALE_UE8M0_PACKED, s.shape[-1], wq, sw, out)
+    torch.cuda.synchronize()
+    if bfq.bfq_poll_device_status() != 0:
+        raise RuntimeError("device status set")
 
 
 def step(bfq, shapes, events=None):
@@ -955,6 +979,9 @@ def run_gpu(args, rank, world, local_rank):
     if args.moe_only:  # profiling mode: the MoE expert slice only, no report
         measure_moe(bfq, torch, dev, hbm_peak, fp8_peak, 2)
         return 0
+    if args.shape and args.ue8m0:  # profiling mode: one shape on the block-scaled arm
+        profile_ue8m0_shape(bfq, torch, dev, args.shape, args.warmup + args.steps)
+        return 0
     shapes = build_problem(bfq, torch, dev, args.shape)
     n_shapes = len(shapes)
     flops_step = sum(2 * s["m"] * s["n"] * s["k"] for s in shapes)
@@ -1139,6 +1166,8 @@ def main(argv=None):
     ap.add_argument("--shape", type=lambda v: tuple(int(t) for t in v.split(",")), default=None,
                     help="m,n,k of one sweep shape: run only it, eagerly, and print nothing "
                          "(for profiler captures)")
+    ap.add_argument("--ue8m0", action="store_true",
+                    help="with --shape: UE8M0 scales on both operands, block-scaled GEMM arm")
     ap.add_argument("--impl", choices=["bfq", "reference"], default="bfq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--moe-only", action="store_true",

@@ -49,9 +49,11 @@ bool pdl_enabled();
 // waits in griddep_wait() before touching memory) and an optional cluster
 // size along x.  With programmatic launch switched off the kernel is
 // launched with plain stream order (griddep_wait() is then a no-op).
+// `programmatic` false: plain stream order whatever the switch says.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                              cudaStream_t stream, unsigned cluster_x, Args&&... args) {
+inline cudaError_t launch_kernel(bool programmatic, void (*kernel)(KArgs...), dim3 grid,
+                                 dim3 block, size_t smem, cudaStream_t stream,
+                                 unsigned cluster_x, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -59,7 +61,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   unsigned n = 0;
-  if (pdl_enabled()) {
+  if (programmatic && pdl_enabled()) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
@@ -74,6 +76,13 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, unsigned cluster_x, Args&&... args) {
+  return launch_kernel(true, kernel, grid, block, smem, stream, cluster_x,
+                       std::forward<Args>(args)...);
 }
 
 // silu(g) of every bf16 gate g (indexed by its 16 bits), evaluated once per

@@ -20,12 +20,14 @@
  *    library allocates nothing and frees nothing; it keeps no per-call state.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Work is enqueued asynchronously on it; the function returns as
- *    soon as the launch is enqueued.  Kernels are launched with programmatic
- *    stream serialization: a kernel may be scheduled while the previous one in
- *    the stream is finishing, but it waits for that kernel's completion (and
- *    memory visibility) before it reads or writes any global memory, so
- *    stream order semantics are unchanged.  Launches can be captured in CUDA
- *    graphs.
+ *    soon as the launch is enqueued.  GEMM kernels, and quant and
+ *    silu-mul-quant grids that fit in one wave, are launched with
+ *    programmatic stream serialization: a kernel may be scheduled while the
+ *    previous one in the stream is finishing, but it waits for that kernel's
+ *    completion (and memory visibility) before it reads or writes any global
+ *    memory, so stream order semantics are unchanged.  (Multi-wave quant
+ *    grids keep plain stream order: launched early they slowed a sequence of
+ *    GEMMs.)  Launches can be captured in CUDA graphs.
  *  - Arguments are validated on the host before anything is launched; an
  *    invalid call launches nothing and returns a non-zero bfq_status.  There
  *    is no CPU fallback and no alternative backend.
@@ -425,9 +427,9 @@ bfq_status bfq_gemm_block_fp8_masked_silu_quant_ue8m0(
 /*
  * Process-wide switch for programmatic dependent launch ([DG-bench] §4.2: the
  * GEMM wrapper enables PDL so that a kernel's set-up overlaps the tail of the
- * kernel before it).  enable != 0 (the default): every kernel is launched
- * with programmatic stream serialization, as described in the conventions
- * above.  enable == 0: plain stream order, each kernel scheduled only after
+ * kernel before it).  enable != 0 (the default): kernels are launched with
+ * programmatic stream serialization as described in the conventions above.
+ * enable == 0: plain stream order for every kernel, each scheduled only after
  * the previous one has finished.  Results are bit-identical either way; the
  * switch exists to measure what the overlap buys.  It applies to launches
  * made (or captured into a graph) after the call.  Returns the previous
