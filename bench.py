@@ -89,16 +89,20 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# The sources of the sweep's GEMM kernels, whose DRAM traffic the committed
+# profile records.
+KERNEL_SOURCES = ("block_scaled_fp8_quant_gb300/csrc/gemm_kernels.cu",
+                  "block_scaled_fp8_quant_gb300/csrc/gemm_common.cuh",
+                  "block_scaled_fp8_quant_gb300/csrc/bfq_device.cuh")
+
+
 def kernel_source_hash():
     """Hash of the kernel sources' code: comments, trailing blanks and empty
     lines are left out, so that a comment edit keeps the measured profile."""
     import re
 
     h = hashlib.sha256()
-    for rel in ("block_scaled_fp8_quant_gb300/csrc/gemm_kernels.cu",
-                "block_scaled_fp8_quant_gb300/csrc/gemm_common.cuh",
-                "block_scaled_fp8_quant_gb300/csrc/bfq_device.cuh",
-                "block_scaled_fp8_quant_gb300/csrc/quant_kernels.cu"):
+    for rel in KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
             src = f.read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)

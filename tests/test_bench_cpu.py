@@ -55,8 +55,8 @@ def test_kernel_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
 
     csrc = tmp_path / "block_scaled_fp8_quant_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    for f in ("gemm_kernels.cu", "bfq_device.cuh", "quant_kernels.cu"):
-        shutil.copy(os.path.join(ROOT, "block_scaled_fp8_quant_gb300", "csrc", f), csrc / f)
+    for rel in bench.KERNEL_SOURCES:
+        shutil.copy(os.path.join(ROOT, rel), tmp_path / rel)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h0 = bench.kernel_source_hash()
     g = csrc / "gemm_kernels.cu"
