@@ -41,20 +41,30 @@ class BfqError(RuntimeError):
         self.status = status
 
 
+_debug = False
+
+
 def library_path() -> str:
-    return os.path.join(_HERE, "libbfq.so")
+    return os.path.join(_HERE, "libbfq_debug.so" if _debug else "libbfq.so")
 
 
-def load_library(build: bool = True):
-    """Load libbfq.so (building it in-tree first when stale); raise if impossible."""
-    global _lib
+def load_library(build: bool = True, debug: bool | None = None):
+    """Load libbfq.so (building it in-tree first when stale); raise if impossible.
+    debug=True (before the first load of the process): libbfq_debug.so, the
+    build whose kernels check their memory accesses against the arrays'
+    extents and latch BFQ_ERR_DEVICE_BOUNDS (read by bfq_poll_device_status).
+    debug=None: the library already loaded, else the release build."""
+    global _lib, _debug
     with _lock:
         if _lib is not None:
+            if debug is not None and debug != _debug:
+                raise RuntimeError("the other build of the library is already loaded")
             return _lib
+        _debug = bool(debug)
         if build:
             from . import _build
 
-            _build.build()
+            _build.build(debug=_debug)
         path = library_path()
         if not os.path.exists(path):
             raise RuntimeError(f"libbfq.so not found at {path}: build the CUDA library first")

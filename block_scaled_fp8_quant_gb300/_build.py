@@ -18,6 +18,11 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbfq.so")
+# The debug build: the same sources with BFQ_DEVICE_CHECKS, whose kernels
+# check every computed global offset against its array's extent and latch
+# BFQ_ERR_DEVICE_BOUNDS instead of accessing out of bounds.
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libbfq_debug.so")
 SOURCES = ["bfq_api.cu", "quant_kernels.cu", "gemm_kernels.cu", "gemm_blockscaled.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -44,9 +49,10 @@ def _deps() -> list[str]:
     return files
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [_nvcc()] + _flags() + ["-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, verbose: bool, debug: bool = False) -> str:
+    obj = os.path.join(BUILD_DEBUG if debug else BUILD, os.path.splitext(src)[0] + ".o")
+    cmd = [_nvcc()] + _flags() + (["-DBFQ_DEVICE_CHECKS"] if debug else []) + [
+        "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -57,22 +63,25 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of libbfq.so."""
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile (if stale) and return the path of libbfq.so (debug=True: of
+    libbfq_debug.so, the build with device bounds checks)."""
+    lib = LIB_DEBUG if debug else LIB
     newest = max(os.path.getmtime(f) for f in _deps())
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= newest:
+        return lib
+    os.makedirs(BUILD_DEBUG if debug else BUILD, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    tmp = LIB + f".{os.getpid()}.tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose, debug), SOURCES))
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [_nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart_static"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -109,6 +109,7 @@ extern "C" const char* bfq_status_string(bfq_status status) {
     case BFQ_ERR_TIMEOUT: return "BFQ_ERR_TIMEOUT";
     case BFQ_ERR_WORKSPACE: return "BFQ_ERR_WORKSPACE";
     case BFQ_ERR_DEVICE: return "BFQ_ERR_DEVICE";
+    case BFQ_ERR_DEVICE_BOUNDS: return "BFQ_ERR_DEVICE_BOUNDS";
     default: return "BFQ_ERR_UNKNOWN";
   }
 }

@@ -31,6 +31,22 @@ __device__ __forceinline__ void record_timeout(int* status) {
   atomicExch(status, BFQ_ERR_TIMEOUT);
 }
 
+// Debug builds (compiled with BFQ_DEVICE_CHECKS): every global access whose
+// offset the kernel computes checks it against the extent of its array, as
+// the host derived it from the call's arguments; a failing check latches
+// BFQ_ERR_DEVICE_BOUNDS in the status word (never overwriting an earlier
+// error) and the access is skipped.  Release builds compile the checks away.
+#ifdef BFQ_DEVICE_CHECKS
+__device__ __forceinline__ bool in_bounds(int* status, int64_t off, int64_t len,
+                                          int64_t extent) {
+  if (off >= 0 && off + len <= extent) return true;
+  atomicCAS(status, 0, BFQ_ERR_DEVICE_BOUNDS);
+  return false;
+}
+#else
+__device__ __forceinline__ bool in_bounds(int*, int64_t, int64_t, int64_t) { return true; }
+#endif
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -303,8 +303,10 @@ __global__ void __launch_bounds__(BsCfg::kThreads, 1)
       const int nb0 = c_ld.n0 / 128;
       if (!wbulk) {
         const int nb = nb0 + (lane >> 2), kb = i0 + (lane & 3);
-        f.w = (lane < 8 && nb < nblks && kb < KB) ? __float_as_uint(__ldg(sw + (int64_t)nb * KB + kb))
-                                                  : 0x3F800000u;
+        f.w = (lane < 8 && nb < nblks && kb < KB &&
+               in_bounds(p.status, (sw - p.sw) + (int64_t)nb * KB + kb, 1, p.n_sw))
+                  ? __float_as_uint(__ldg(sw + (int64_t)nb * KB + kb))
+                  : 0x3F800000u;
       }
       if (!packed) {
 #pragma unroll
@@ -313,7 +315,11 @@ __global__ void __launch_bounds__(BsCfg::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             f.a[4 * c + k] =
-                (m < c_ld.ml && k < nk) ? __ldg(sa + (int64_t)(i0 + k) * p.sa_ld + m) : 0x3F800000u;
+                (m < c_ld.ml && k < nk &&
+                 in_bounds(p.status, (sa - (const uint32_t*)p.sa) + (int64_t)(i0 + k) * p.sa_ld + m,
+                           1, p.n_sa))
+                    ? __ldg(sa + (int64_t)(i0 + k) * p.sa_ld + m)
+                    : 0x3F800000u;
         }
       }
       if (!bulk) return true;
@@ -325,10 +331,18 @@ __global__ void __launch_bounds__(BsCfg::kThreads, 1)
         if (ok) {
           uint32_t* wa = sf + slot * C::kSfSlotWords;
           // rows m0 .. of the group's word column, not past the column's end
-          const uint32_t abytes = packed ? (uint32_t)min(kBM, (int)(p.sa_ld - c_ld.m0)) * 4u : 0u;
-          const int nbw = wbulk ? min(2, nblks - nb0) : 0;
+          uint32_t abytes = packed ? (uint32_t)min(kBM, (int)(p.sa_ld - c_ld.m0)) * 4u : 0u;
+          int nbw = wbulk ? min(2, nblks - nb0) : 0;
+          if (packed && !in_bounds(p.status,
+                                   (sa - (const uint32_t*)p.sa) + (int64_t)(i0 >> 2) * p.sa_ld +
+                                       c_ld.m0,
+                                   abytes / 4, p.n_sa))
+            abytes = 0;
+          if (nbw > 0 && !in_bounds(p.status, (sw - p.sw) + (int64_t)nb0 * KB + i0,
+                                    (int64_t)(nbw - 1) * KB + 4, p.n_sw))
+            nbw = 0;
           mbar_arrive_expect_tx(&sload[slot], abytes + 16u * (uint32_t)nbw);
-          if (packed)
+          if (abytes)
             bulk_load_1d(wa, sa + (int64_t)(i0 >> 2) * p.sa_ld + c_ld.m0, abytes, &sload[slot]);
           for (int h = 0; h < nbw; ++h)
             bulk_load_1d(wa + C::kSfSlotWords - 8 + 4 * h, sw + (int64_t)(nb0 + h) * KB + i0, 16u,
@@ -503,8 +517,9 @@ __global__ void __launch_bounds__(BsCfg::kThreads, 1)
           const uint32_t box = smem_u32(stg);
           for (int x = tid; x < rows_valid * 8; x += C::kEpiWarps * 32) {
             const int r = x >> 3, c = x & 7;
-            st_v4(base + (int64_t)r * p.N + c * 8,
-                  ld_shared_v4(box + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4))));
+            if (in_bounds(p.status, (base - p.out) + (int64_t)r * p.N + c * 8, 8, p.n_out))
+              st_v4(base + (int64_t)r * p.N + c * 8,
+                    ld_shared_v4(box + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4))));
           }
         }
       }
@@ -614,6 +629,9 @@ extern "C" bfq_status bfq_gemm_block_fp8_ue8m0(const void* a_q, const void* a_sc
   p.n_tiles = (int)cdiv(N, BsCfg::kBN);
   p.splits = 1;
   p.a_fmt = a_fmt;
+  p.n_sa = scale_cols(K, a_fmt) * a_scale_ld;
+  p.n_sw = cdiv(N, 128) * (K / 128);
+  p.n_out = M * N;
   return launch_bs<false>(dev, ma, mw, mo, p, (int64_t)p.m_tiles * p.n_tiles,
                           (cudaStream_t)stream);
 }
@@ -662,6 +680,9 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked_ue8m0(
   p.splits = 1;
   p.a_fmt = a_fmt;
   p.E = E;
+  p.n_sa = E * p.sa_estride;
+  p.n_sw = E * p.sw_estride;
+  p.n_out = (int64_t)E * T * N;
   return launch_bs<true>(dev, ma, mw, mw, p, (int64_t)p.m_tiles * p.n_tiles * E,
                          (cudaStream_t)stream);
 }
@@ -716,6 +737,10 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked_silu_quant_ue8m0(
   p.q_scale_ld = q_scale_ld;
   p.q_fmt = q_fmt;
   p.silu_tab = silu_table(dev, (cudaStream_t)stream);
+  p.n_sa = E * p.sa_estride;
+  p.n_sw = E * p.sw_estride;
+  p.n_q = (int64_t)E * T * I;
+  p.n_qs = E * scale_cols(I, q_fmt) * q_scale_ld;
   return launch_bs<true, true>(dev, ma, mw, mw, p, (int64_t)p.m_tiles * p.n_tiles * E,
                                (cudaStream_t)stream);
 }

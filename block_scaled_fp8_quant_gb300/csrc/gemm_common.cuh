@@ -40,6 +40,9 @@ struct GemmParams {
   // fused silu-mul-quant (SILU kernel): silu of every bf16 gate, indexed by
   // its 16 bits (the library's table), or null to compute it
   const float* silu_tab;
+  // extents of the arrays, in their elements (32-bit scale words / floats,
+  // bf16 outputs, e4m3 codes), for the debug build's bounds checks
+  int64_t n_sa, n_sw, n_out, n_q, n_qs;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -156,7 +159,9 @@ __device__ __forceinline__ void silu_quant_tile_rows(const GemmParams& p, uint64
   float sc = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
   if (p.q_fmt != BFQ_SCALE_F32) sc = ceil_pow2(sc);
   const float y_inv = __frcp_rn(sc);
-  uint8_t* qrow = p.q_out + ((int64_t)e * p.M + m) * I + fg * 128 + half * 64;
+  const int64_t qoff = ((int64_t)e * p.M + m) * I + fg * 128 + half * 64;
+  uint8_t* qrow = p.q_out + qoff;
+  const bool q_ok = in_bounds(p.status, qoff, 64, p.n_q);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {  // 16 codes per 16-byte store
     uint32_t w[4];
@@ -173,19 +178,22 @@ __device__ __forceinline__ void silu_quant_tile_rows(const GemmParams& p, uint64
       }
       w[t] = lo | (hi << 16);
     }
-    st_v4(qrow + c * 16, make_uint4(w[0], w[1], w[2], w[3]));
+    if (q_ok) st_v4(qrow + c * 16, make_uint4(w[0], w[1], w[2], w[3]));
   }
   if (half == 0) {
     const int G = I >> 7;
     if (p.q_fmt == BFQ_SCALE_UE8M0_PACKED) {
       const int64_t cols = (G + 3) >> 2;
-      uint8_t* word =
-          (uint8_t*)p.q_scales + (((int64_t)e * cols + (fg >> 2)) * p.q_scale_ld + m) * 4;
-      word[fg & 3] = (uint8_t)ue8m0_byte(sc);
-      if (fg == G - 1)
-        for (int b = (fg & 3) + 1; b < 4; ++b) word[b] = 0;
+      const int64_t woff = ((int64_t)e * cols + (fg >> 2)) * p.q_scale_ld + m;
+      if (in_bounds(p.status, woff, 1, p.n_qs)) {
+        uint8_t* word = (uint8_t*)p.q_scales + woff * 4;
+        word[fg & 3] = (uint8_t)ue8m0_byte(sc);
+        if (fg == G - 1)
+          for (int b = (fg & 3) + 1; b < 4; ++b) word[b] = 0;
+      }
     } else {
-      ((float*)p.q_scales)[((int64_t)e * G + fg) * p.q_scale_ld + m] = sc;
+      const int64_t soff = ((int64_t)e * G + fg) * p.q_scale_ld + m;
+      if (in_bounds(p.status, soff, 1, p.n_qs)) ((float*)p.q_scales)[soff] = sc;
     }
   }
 }

@@ -77,11 +77,16 @@ struct GemmCfg {
 // correctly rounded quotient, saturating e4m3 — so the codes and scales are
 // those of quantizing the stored bf16 output ("[Perf] Deepgemm fused layout
 // kernel for activations": no separate quant or layout pass).
-//   q_row   &q_out[m][col0];  group = col0 / 128;  last = this is the row's
-//   last group (a packed word it leaves incomplete gets zero bytes).
-__device__ __forceinline__ void quant_store_row_group(const uint64_t (&acc)[64], uint8_t* q_row,
-                                                      void* scales, int64_t ld, int m, int group,
-                                                      bool last, int fmt) {
+//   row m, columns col0 .. col0 + 127 of q_out; group = col0 / 128; the
+//   row's last group zeroes the bytes a partial packed word leaves unused.
+__device__ __forceinline__ void quant_store_row_group(const uint64_t (&acc)[64],
+                                                      const GemmParams& p, int m, int col0) {
+  const int fmt = p.q_fmt, group = col0 >> 7;
+  const bool last = col0 + 128 >= p.N;
+  const int64_t ld = p.q_scale_ld;
+  const int64_t qoff = (int64_t)m * p.N + col0;
+  uint8_t* q_row = p.q_out + qoff;
+  const bool q_ok = in_bounds(p.status, qoff, 128, p.n_q);
   float amax = 0.0f;
 #pragma unroll
   for (int j = 0; j < 64; ++j) {
@@ -110,15 +115,18 @@ __device__ __forceinline__ void quant_store_row_group(const uint64_t (&acc)[64],
       }
       w[t] = lo | (hi << 16);
     }
-    st_v4(q_row + c * 16, make_uint4(w[0], w[1], w[2], w[3]));
+    if (q_ok) st_v4(q_row + c * 16, make_uint4(w[0], w[1], w[2], w[3]));
   }
   if (fmt == BFQ_SCALE_UE8M0_PACKED) {
-    uint8_t* word = (uint8_t*)scales + ((int64_t)(group >> 2) * ld + m) * 4;
+    const int64_t woff = (int64_t)(group >> 2) * ld + m;
+    if (!in_bounds(p.status, woff, 1, p.n_qs)) return;
+    uint8_t* word = (uint8_t*)p.q_scales + woff * 4;
     word[group & 3] = (uint8_t)ue8m0_byte(s);
     if (last)
       for (int b = (group & 3) + 1; b < 4; ++b) word[b] = 0;
   } else {
-    ((float*)scales)[(int64_t)group * ld + m] = s;
+    const int64_t soff = (int64_t)group * ld + m;
+    if (in_bounds(p.status, soff, 1, p.n_qs)) ((float*)p.q_scales)[soff] = s;
   }
 }
 
@@ -280,11 +288,16 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
         const uint32_t ph = (uint32_t)(i / C::kScaleSlots) & 1u;
         if (!mbar_wait(&sempty[slot], ph ^ 1u, abort_flag, p.status, kWaitTimeoutNs)) break;
         const int kb = kb_begin + i;
+        const int64_t col_off = (MASKED ? (int64_t)e * p.sa_estride : 0) +
+                                (int64_t)(packed ? (kb >> 2) : kb) * p.sa_ld + m0;
+        const int64_t w_off = (MASKED ? (int64_t)e * p.sw_estride : 0) +
+                              (int64_t)(nb0 + lane) * KBs + kb;
         const uint32_t* col = (const uint32_t*)sa + (int64_t)(packed ? (kb >> 2) : kb) * p.sa_ld;
   #pragma unroll
         for (int r = lane; r < kBM; r += 32)
-          if (m0 + r < m_limit) cp_async_4(&sc_a[slot * kBM + r], col + m0 + r);
-        if (lane < BN / 128 && nb0 + lane < nblks)
+          if (m0 + r < m_limit && in_bounds(p.status, col_off + r, 1, p.n_sa))
+            cp_async_4(&sc_a[slot * kBM + r], col + m0 + r);
+        if (lane < BN / 128 && nb0 + lane < nblks && in_bounds(p.status, w_off, 1, p.n_sw))
           cp_async_4(&sc_w[slot * 2 + lane], sw + (int64_t)(nb0 + lane) * KBs + kb);
         cp_async_arrive_noinc(&sfull[slot]);
       }
@@ -386,8 +399,7 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
       }
       if constexpr (QOUT) {
         if (ok && warp_active && row_ok)
-          quant_store_row_group(acc, p.q_out + (int64_t)m * p.N + col0, p.q_scales, p.q_scale_ld,
-                                m, col0 >> 7, col0 + 128 >= p.N, p.q_fmt);
+          quant_store_row_group(acc, p, m, col0);
       }
     } else if (p.splits == 1) {
       if (ok && warp_active && row_ok) {
@@ -397,8 +409,9 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
           if (c * 8 < ncols) {
             const float2 f0 = unpack2(acc[c * 4 + 0]), f1 = unpack2(acc[c * 4 + 1]);
             const float2 f2 = unpack2(acc[c * 4 + 2]), f3 = unpack2(acc[c * 4 + 3]);
-            st_v4(dst + c * 8, make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
-                                          pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
+            if (in_bounds(p.status, out_row + col0 + c * 8, 8, p.n_out))
+              st_v4(dst + c * 8, make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
+                                            pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y)));
           }
         }
       }
@@ -473,7 +486,8 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
           const int64_t off = (int64_t)(m0 + r) * p.N + col + lane * 4;
           const float4 a4 = sum_parts(v);
           const uint32_t b01 = pack_bf16x2(a4.x, a4.y), b23 = pack_bf16x2(a4.z, a4.w);
-          if (p.out) *reinterpret_cast<uint2*>(p.out + off) = make_uint2(b01, b23);
+          if (p.out && in_bounds(p.status, off, 4, p.n_out))
+            *reinterpret_cast<uint2*>(p.out + off) = make_uint2(b01, b23);
           const float x0 = bf16lo(b01), x1 = bf16hi(b01), x2 = bf16lo(b23), x3 = bf16hi(b23);
           float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
 #pragma unroll
@@ -490,17 +504,21 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
             lo = cvt_e4m3x2(__fmul_rn(x0, y), __fmul_rn(x1, y));
             hi = cvt_e4m3x2(__fmul_rn(x2, y), __fmul_rn(x3, y));
           }
-          *reinterpret_cast<uint32_t*>(p.q_out + off) = lo | (hi << 16);
+          if (in_bounds(p.status, off, 4, p.n_q))
+            *reinterpret_cast<uint32_t*>(p.q_out + off) = lo | (hi << 16);
           if (lane == 0) {
             const int m = m0 + r, group = col >> 7;
             if (p.q_fmt == BFQ_SCALE_UE8M0_PACKED) {
-              uint8_t* word =
-                  (uint8_t*)p.q_scales + ((int64_t)(group >> 2) * p.q_scale_ld + m) * 4;
-              word[group & 3] = (uint8_t)ue8m0_byte(sc);
-              if (col + 128 >= p.N)
-                for (int bb = (group & 3) + 1; bb < 4; ++bb) word[bb] = 0;
+              const int64_t woff = (int64_t)(group >> 2) * p.q_scale_ld + m;
+              if (in_bounds(p.status, woff, 1, p.n_qs)) {
+                uint8_t* word = (uint8_t*)p.q_scales + woff * 4;
+                word[group & 3] = (uint8_t)ue8m0_byte(sc);
+                if (col + 128 >= p.N)
+                  for (int bb = (group & 3) + 1; bb < 4; ++bb) word[bb] = 0;
+              }
             } else {
-              ((float*)p.q_scales)[(int64_t)group * p.q_scale_ld + m] = sc;
+              const int64_t soff = (int64_t)group * p.q_scale_ld + m;
+              if (in_bounds(p.status, soff, 1, p.n_qs)) ((float*)p.q_scales)[soff] = sc;
             }
           }
         }
@@ -517,8 +535,9 @@ __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
           float4 v[kMaxSplits];
           load_parts(r, c4, v);
           const float4 a4 = sum_parts(v);
-          *reinterpret_cast<uint2*>(p.out + off) =
-              make_uint2(pack_bf16x2(a4.x, a4.y), pack_bf16x2(a4.z, a4.w));
+          if (in_bounds(p.status, off, 4, p.n_out))
+            *reinterpret_cast<uint2*>(p.out + off) =
+                make_uint2(pack_bf16x2(a4.x, a4.y), pack_bf16x2(a4.z, a4.w));
         }
       }
       cluster_sync();  // the peers have read this CTA's partial
@@ -741,8 +760,10 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
         const uint32_t* col = sa + (int64_t)(packed ? (i >> 2) : i) * p.sa_ld;
 #pragma unroll
         for (int r = lane; r < kBM; r += 32)
-          if (m0 + r < ml) cp_async_4(&sc_a[slot * kBM + r], col + m0 + r);
-        if (lane < 2 && nb0 + lane < nblks)
+          if (m0 + r < ml && in_bounds(p.status, (col - (const uint32_t*)p.sa) + m0 + r, 1, p.n_sa))
+            cp_async_4(&sc_a[slot * kBM + r], col + m0 + r);
+        if (lane < 2 && nb0 + lane < nblks &&
+            in_bounds(p.status, (sw - p.sw) + (int64_t)(nb0 + lane) * KB + i, 1, p.n_sw))
           cp_async_4(&sc_w[slot * 2 + lane], sw + (int64_t)(nb0 + lane) * KB + i);
         cp_async_arrive_noinc(&sfull[slot]);
         if (++i == KB) {
@@ -880,8 +901,9 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
                 p.out + (int64_t)e * p.out_estride + (int64_t)m0 * p.N + n0 + b * 64;
             for (int q = tid; q < rows_valid * 8; q += C::kEpiWarps * 32) {
               const int r = q >> 3, c = q & 7;
-              st_v4(base + (int64_t)r * p.N + c * 8,
-                    ld_shared_v4(box + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4))));
+              if (in_bounds(p.status, (base - p.out) + (int64_t)r * p.N + c * 8, 8, p.n_out))
+                st_v4(base + (int64_t)r * p.N + c * 8,
+                      ld_shared_v4(box + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4))));
             }
           }
         }
@@ -909,8 +931,7 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
         }
         if constexpr (QOUT) {
           if (warp_active && row_ok)
-            quant_store_row_group(acc, p.q_out + (int64_t)m * p.N + col0, p.q_scales,
-                                  p.q_scale_ld, m, col0 >> 7, col0 + 128 >= p.N, p.q_fmt);
+            quant_store_row_group(acc, p, m, col0);
         }
       }
     }
@@ -1256,6 +1277,11 @@ bfq_status gemm_dense(const void* a_q, const void* a_scales, int32_t a_fmt, int6
     p.q_scale_ld = qo->scale_ld;
     p.q_fmt = qo->fmt;
   }
+  p.n_sa = scale_cols(K, a_fmt) * a_scale_ld;
+  p.n_sw = cdiv(N, 128) * (K / 128);
+  p.n_out = M * N;
+  p.n_q = qo ? M * N : 0;
+  p.n_qs = qo ? scale_cols(N, qo->fmt) * qo->scale_ld : 0;
   const unsigned grid = (unsigned)(pl.m_tiles * pl.n_tiles * pl.splits);
   const unsigned pgrid = grid < (unsigned)dev.sm_count ? grid : (unsigned)dev.sm_count;
   cudaStream_t s = (cudaStream_t)stream;
@@ -1340,6 +1366,9 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked(
   p.splits = 1;
   p.a_fmt = a_fmt;
   p.E = E;
+  p.n_sa = E * p.sa_estride;
+  p.n_sw = E * p.sw_estride;
+  p.n_out = (int64_t)E * T * N;
   const int64_t grid = (int64_t)p.m_tiles * p.n_tiles * E;
   if (grid > 0x7FFFFFFF) return BFQ_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;
@@ -1471,6 +1500,10 @@ extern "C" bfq_status bfq_gemm_block_fp8_masked_silu_quant(
   p.q_scale_ld = q_scale_ld;
   p.q_fmt = q_fmt;
   p.silu_tab = silu_table(dev, (cudaStream_t)stream);
+  p.n_sa = E * p.sa_estride;
+  p.n_sw = E * p.sw_estride;
+  p.n_q = (int64_t)E * T * I;
+  p.n_qs = E * scale_cols(I, q_fmt) * q_scale_ld;
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles * E;
   const unsigned grid = (unsigned)(tiles < dev.sm_count ? tiles : dev.sm_count);
   return launch_persistent<true, false, true>(dev, ma, mw, mw, p, grid, (cudaStream_t)stream);

@@ -70,21 +70,25 @@ __device__ __forceinline__ float quant16(const float (&v)[16], uint4& codes) {
 
 // Write the scales of one chunk (4 groups) of row r.  Lanes 0, 8, 16, 24
 // hold the scales of groups 0..3 of the chunk.
+// (status, base_off, n_s: the debug build's bounds check of the scale
+// array, base_off = the offset of `scales` within it.)
 template <int FMT>
 __device__ __forceinline__ void store_chunk_scales(float s, bool gactive, int lane,
                                                    int64_t chunk, int64_t r, void* scales,
-                                                   int64_t ld) {
+                                                   int64_t ld, int* status, int64_t base_off,
+                                                   int64_t n_s) {
   if (FMT == BFQ_SCALE_UE8M0_PACKED) {
     uint32_t b = gactive ? ue8m0_byte(s) : 0u;
     uint32_t b0 = __shfl_sync(0xFFFFFFFFu, b, 0);
     uint32_t b1 = __shfl_sync(0xFFFFFFFFu, b, 8);
     uint32_t b2 = __shfl_sync(0xFFFFFFFFu, b, 16);
     uint32_t b3 = __shfl_sync(0xFFFFFFFFu, b, 24);
-    if (lane == 0)
+    if (lane == 0 && in_bounds(status, base_off + chunk * ld + r, 1, n_s))
       ((uint32_t*)scales)[chunk * ld + r] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
   } else {
-    if (gactive && (lane & 7) == 0)
-      ((float*)scales)[(chunk * 4 + (lane >> 3)) * ld + r] = s;
+    const int64_t off = (chunk * 4 + (lane >> 3)) * ld + r;
+    if (gactive && (lane & 7) == 0 && in_bounds(status, base_off + off, 1, n_s))
+      ((float*)scales)[off] = s;
   }
 }
 
@@ -103,7 +107,8 @@ __device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float (
 template <int FMT>
 __global__ void __launch_bounds__(kQuantWarps * 32)
     quant_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K, int64_t ld_x,
-                 uint8_t* __restrict__ q, void* __restrict__ scales, int64_t scale_ld) {
+                 uint8_t* __restrict__ q, void* __restrict__ scales, int64_t scale_ld,
+                 int* status, int64_t n_x, int64_t n_s) {
   griddep_wait();
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
@@ -121,7 +126,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     for (int j = 0; j < kUnroll; ++j) {
       const int64_t u = u0 + j;
       const int64_t r = u / chunks, c = u - (u / chunks) * chunks;
-      act[j] = (u < units) && (c * 4 + gl < G);
+      act[j] = (u < units) && (c * 4 + gl < G) &&
+               in_bounds(status, r * ld_x + c * 512 + lane * 16, 16, n_x);
       if (act[j]) {
         const __nv_bfloat16* p = x + r * ld_x + c * 512 + lane * 16;
         raw[j][0] = ld_stream_v4(p);
@@ -140,8 +146,9 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       unpack16(raw[j][0], raw[j][1], v);
       uint4 codes;
       const float s = quant16<FMT>(v, codes);
-      if (act[j]) st_v4(q + r * K + c * 512 + lane * 16, codes);
-      store_chunk_scales<FMT>(s, act[j], lane, c, r, scales, scale_ld);
+      if (act[j] && in_bounds(status, r * K + c * 512 + lane * 16, 16, M * K))
+        st_v4(q + r * K + c * 512 + lane * 16, codes);
+      store_chunk_scales<FMT>(s, act[j], lane, c, r, scales, scale_ld, status, 0, n_s);
     }
   }
 }
@@ -172,7 +179,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int I,
                           const int32_t* __restrict__ counts, uint8_t* __restrict__ q,
                           void* __restrict__ scales, int64_t scale_ld,
-                          const float* __restrict__ silu_tab) {
+                          const float* __restrict__ silu_tab, int* status, int64_t n_x,
+                          int64_t n_s) {
   griddep_wait();
   griddep_launch_dependents();
   const int e = blockIdx.y;
@@ -199,7 +207,10 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     for (int j = 0; j < kSiluUnroll; ++j) {
       const int u = u0 + j;
       const int r = r0 + u / chunks, c = u % chunks;
-      act[j] = (u < units) && (c * 4 + gl < G);
+      act[j] = (u < units) && (c * 4 + gl < G) &&
+               in_bounds(status,
+                         ((int64_t)e * T + r) * (2 * (int64_t)I) + c * 512 + lane * 16 + I, 16,
+                         n_x);
       if (act[j]) {
         const __nv_bfloat16* p = x + ((int64_t)e * T + r) * (2 * (int64_t)I) + c * 512 + lane * 16;
         raw[j][0] = ld_stream_v4(p);
@@ -236,8 +247,10 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       }
       uint4 codes;
       const float s = quant16<FMT>(y, codes);
-      if (act[j]) st_v4(q + ((int64_t)e * T + r) * I + c * 512 + lane * 16, codes);
-      store_chunk_scales<FMT>(s, act[j], lane, c, r, sc_e, scale_ld);
+      const int64_t qoff = ((int64_t)e * T + r) * I + c * 512 + lane * 16;
+      if (act[j] && in_bounds(status, qoff, 16, n_x / 2)) st_v4(q + qoff, codes);
+      store_chunk_scales<FMT>(s, act[j], lane, c, r, sc_e, scale_ld, status,
+                              (int64_t)e * cols * scale_ld, n_s);
     }
   }
 }
@@ -249,7 +262,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 template <bool POW2>
 __global__ void __launch_bounds__(256)
     weight_quant_kernel(const __nv_bfloat16* __restrict__ w, int64_t N, int64_t K,
-                        uint8_t* __restrict__ wq, float* __restrict__ sw) {
+                        uint8_t* __restrict__ wq, float* __restrict__ sw, int* status,
+                        int64_t n_w, int64_t n_s) {
   __shared__ float red[8];
   griddep_wait();
   griddep_launch_dependents();
@@ -257,7 +271,7 @@ __global__ void __launch_bounds__(256)
   const int64_t nb = blockIdx.y, kb = blockIdx.x, b = blockIdx.z;
   const int t = threadIdx.x;
   const int64_t n = nb * 128 + (t >> 1);
-  const bool row_ok = n < N;
+  const bool row_ok = n < N && in_bounds(status, (b * N + n) * K + kb * 128 + (t & 1) * 64, 64, n_w);
   const __nv_bfloat16* src = w + (b * N + n) * K + kb * 128 + (t & 1) * 64;
   uint4 raw[8];
 #pragma unroll
@@ -281,7 +295,7 @@ __global__ void __launch_bounds__(256)
   float s = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
   if (POW2) s = ceil_pow2(s);
   const float y = __frcp_rn(s);
-  if (t == 0) sw[(b * NB + nb) * KB + kb] = s;
+  if (t == 0 && in_bounds(status, (b * NB + nb) * KB + kb, 1, n_s)) sw[(b * NB + nb) * KB + kb] = s;
   if (!row_ok) return;
   uint8_t* dst = wq + (b * N + n) * K + kb * 128 + (t & 1) * 64;
 #pragma unroll
@@ -362,24 +376,28 @@ extern "C" bfq_status bfq_quant(const void* x, int64_t M, int64_t K, int64_t ld_
   cudaStream_t s = (cudaStream_t)stream;
   const auto* xb = (const __nv_bfloat16*)x;
   auto* qb = (uint8_t*)q;
+  int* status = device_status_ptr();
+  if (!status) return BFQ_ERR_CUDA;
+  const int64_t n_x = (M - 1) * ld_x + K;           // extents for the debug bounds checks
+  const int64_t n_s = scale_cols(K, fmt) * scale_ld;
   switch (fmt) {
     case BFQ_SCALE_F32:
       st = launch_status(launch_kernel(one_wave(quant_kernel<BFQ_SCALE_F32>, dev, blocks),
                                        quant_kernel<BFQ_SCALE_F32>, dim3((unsigned)blocks),
                                     dim3(kQuantWarps * 32), 0, s, 1, xb, M, K, ld_x, qb, scales,
-                                    scale_ld));
+                                    scale_ld, status, n_x, n_s));
       break;
     case BFQ_SCALE_F32_POW2:
       st = launch_status(launch_kernel(one_wave(quant_kernel<BFQ_SCALE_F32_POW2>, dev, blocks),
                                        quant_kernel<BFQ_SCALE_F32_POW2>, dim3((unsigned)blocks),
                                     dim3(kQuantWarps * 32), 0, s, 1, xb, M, K, ld_x, qb, scales,
-                                    scale_ld));
+                                    scale_ld, status, n_x, n_s));
       break;
     default:
       st = launch_status(launch_kernel(one_wave(quant_kernel<BFQ_SCALE_UE8M0_PACKED>, dev, blocks),
                                        quant_kernel<BFQ_SCALE_UE8M0_PACKED>, dim3((unsigned)blocks),
                                     dim3(kQuantWarps * 32), 0, s, 1, xb, M, K, ld_x, qb, scales,
-                                    scale_ld));
+                                    scale_ld, status, n_x, n_s));
       break;
   }
   return st;
@@ -424,15 +442,21 @@ template <int FMT>
 bfq_status launch_silu_mul_quant(const DeviceInfo& dev, dim3 grid, cudaStream_t s,
                                  const __nv_bfloat16* x, int T, int I, const int32_t* counts,
                                  uint8_t* q, void* scales, int64_t scale_ld, const float* tab) {
+  int* status = device_status_ptr();
+  if (!status) return BFQ_ERR_CUDA;
+  // extents for the debug bounds checks: x [E][T][2I], scales [E][cols][scale_ld]
+  const int64_t E = grid.y;
+  const int64_t n_x = E * T * 2 * (int64_t)I;
+  const int64_t n_s = E * scale_cols(I, FMT) * scale_ld;
   if (tab)
     return launch_status(launch_kernel(one_wave(silu_mul_quant_kernel<FMT, true>, dev, grid.x),
                                        silu_mul_quant_kernel<FMT, true>, grid,
                                        dim3(kQuantWarps * 32), 0, s, 1, x, T, I, counts, q,
-                                       scales, scale_ld, tab));
+                                       scales, scale_ld, tab, status, n_x, n_s));
   return launch_status(launch_kernel(one_wave(silu_mul_quant_kernel<FMT, false>, dev, grid.x),
                                      silu_mul_quant_kernel<FMT, false>, grid,
                                      dim3(kQuantWarps * 32), 0, s, 1, x, T, I, counts, q, scales,
-                                     scale_ld, tab));
+                                     scale_ld, tab, status, n_x, n_s));
 }
 
 }  // namespace
@@ -486,9 +510,12 @@ extern "C" bfq_status bfq_weight_block_quant(const void* w, int64_t batch, int64
   cudaStream_t s = (cudaStream_t)stream;
   const auto* wb = (const __nv_bfloat16*)w;
   auto* wqb = (uint8_t*)wq;
+  int* status = device_status_ptr();
+  if (!status) return BFQ_ERR_CUDA;
+  const int64_t n_w = batch * N * K, n_s = batch * NB * KB;  // debug bounds-check extents
   if (fmt == BFQ_SCALE_F32)
     return launch_status(launch_pdl(weight_quant_kernel<false>, grid, dim3(256), 0, s, 1, wb, N,
-                                    K, wqb, sw));
+                                    K, wqb, sw, status, n_w, n_s));
   return launch_status(launch_pdl(weight_quant_kernel<true>, grid, dim3(256), 0, s, 1, wb, N, K,
-                                  wqb, sw));
+                                  wqb, sw, status, n_w, n_s));
 }

@@ -78,7 +78,10 @@ enum {
   BFQ_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed          */
   BFQ_ERR_TIMEOUT = 6,           /* a kernel watchdog gave up waiting          */
   BFQ_ERR_WORKSPACE = 7,         /* unused: no current plan needs a workspace  */
-  BFQ_ERR_DEVICE = 8             /* current device is not sm_100 family        */
+  BFQ_ERR_DEVICE = 8,            /* current device is not sm_100 family        */
+  BFQ_ERR_DEVICE_BOUNDS = 9      /* debug build: a kernel's bounds check failed
+                                    (latched in the device status; the access
+                                    was skipped)                              */
 };
 
 typedef enum {
@@ -443,7 +446,10 @@ int32_t bfq_set_programmatic_launch(int32_t enable);
  * one atomic exchange on the device (a one-thread kernel on `stream`), so a
  * timeout latched by a kernel on another stream is reported by this call or
  * the next one, never lost.  Synchronizes `stream`.
- * Returns BFQ_OK, BFQ_ERR_TIMEOUT, or BFQ_ERR_CUDA.
+ * Returns BFQ_OK or the latched code — BFQ_ERR_TIMEOUT (a watchdog),
+ * BFQ_ERR_FORMAT (a block-scaled GEMM met a scale that is not a power of
+ * two), BFQ_ERR_DEVICE_BOUNDS (libbfq_debug.so only: a kernel's bounds check
+ * failed) — or BFQ_ERR_CUDA.
  */
 bfq_status bfq_poll_device_status(void* stream);
 
