@@ -670,7 +670,7 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
       (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int steps = my_tiles * KB;
   static_assert(PC::kStages <= C::kStages, "barrier slots for the operand ring");
-  static_assert(C::kScaleSlots == 8, "scale ring of 8 slots");
+  static_assert((C::kScaleSlots & (C::kScaleSlots - 1)) == 0, "scale ring of 2^n slots");
 
   if (warp < C::kEpiWarp0) {
     setmaxnreg_dec<PC::kWg0Regs>();
@@ -753,9 +753,9 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
           sw = p.sw + (MASKED ? (int64_t)e * p.sw_estride : 0);
           nb0 = n0 / 128;
         }
-        const int slot = g & 7;
-        if (!mbar_wait(&sempty[slot], ((uint32_t)(g >> 3) & 1u) ^ 1u, abort_flag, p.status,
-                       kWaitTimeoutNs))
+        const int slot = g % C::kScaleSlots;
+        if (!mbar_wait(&sempty[slot], ((uint32_t)(g / C::kScaleSlots) & 1u) ^ 1u, abort_flag,
+                       p.status, kWaitTimeoutNs))
           break;
         const uint32_t* col = sa + (int64_t)(packed ? (i >> 2) : i) * p.sa_ld;
 #pragma unroll
@@ -823,8 +823,8 @@ __global__ void __launch_bounds__(GemmCfg<256>::kThreads, 1)
       for (int i = 0; i < KB; ++i, ++g) {
         const int buf = g & 1;
         const uint32_t tph = (uint32_t)(g >> 1) & 1u;
-        const int slot = g & 7;
-        const uint32_t sph = (uint32_t)(g >> 3) & 1u;
+        const int slot = g % C::kScaleSlots;
+        const uint32_t sph = (uint32_t)(g / C::kScaleSlots) & 1u;
         if (!mbar_wait(&sfull[slot], sph, abort_flag, p.status, kWaitTimeoutNs)) {
           stop = true;
           break;
