@@ -83,3 +83,51 @@ def test_silu_mul_quant_many_experts(cuda_lib, orc, fmt):
     x = synth.masked_activation(E, T, 2 * I, counts, seed=18)
     q, sc = _run(bfq, x, counts, fmt, 4)
     _check(orc, x, counts, q, sc, fmt)
+
+
+def test_silu_mul_quant_gate_binades_in_order(cuda_lib, orc):
+    """Every bf16 gate below 2^100 in magnitude, in bit-pattern order, with
+    up = 1: each 128-group holds one binade of one sign and y is silu(g)
+    itself, so a wrong table entry shows in its group's codes far more often
+    than with random up values (tests/test_silu_table_gpu.py covers every
+    pattern, NaN included, that way)."""
+    bfq = cuda_lib
+    pats = np.arange(65536, dtype=np.uint32)
+    pats = pats[((pats >> 7) & 0xFF) < 227].astype(np.uint16)
+    I = 2048
+    T = -(-len(pats) // I)
+    gate = np.full(T * I, 0x3F80, np.uint16)  # 1.0 after the last pattern
+    gate[:len(pats)] = pats
+    x = torch.empty((1, T, 2 * I), dtype=torch.bfloat16)
+    x[0, :, :I] = torch.from_numpy(gate.view(np.int16)).view(torch.bfloat16).reshape(T, I)
+    x[0, :, I:] = 1.0
+    counts = torch.tensor([T], dtype=torch.int32)
+    ld = -(-T // 4) * 4
+    for fmt in (0, 2):
+        q, sc = _run(bfq, x, counts, fmt, ld)
+        _check(orc, x, counts, q, sc, fmt)
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_silu_mul_quant_large_batch_edges(cuda_lib, orc, fmt):
+    """A batch of many rows per expert (thousands of blocks) with a partial
+    packed word (I/128 = 5 groups), empty experts, a count past T_max and a
+    negative one, padded rows NaN."""
+    bfq = cuda_lib
+    E, T, I = 8, 400, 640
+    counts = torch.tensor([0, 400, 1, 399, -3, 517, 250, 0], dtype=torch.int32)
+    x = synth.masked_activation(E, T, 2 * I, counts.clamp(0, T), seed=31)
+    q, sc = _run(bfq, x, counts, fmt, 400)
+    _check(orc, x, counts, q, sc, fmt)
+
+
+@pytest.mark.parametrize("fmt", [0, 2])
+def test_silu_mul_quant_thousand_small_experts(cuda_lib, orc, fmt):
+    """1000 experts of at most 4 rows, most rows padded."""
+    bfq = cuda_lib
+    E, T, I = 1000, 4, 256
+    g = torch.Generator().manual_seed(41)
+    counts = torch.randint(0, T + 1, (E,), generator=g, dtype=torch.int32)
+    x = synth.masked_activation(E, T, 2 * I, counts, seed=42)
+    q, sc = _run(bfq, x, counts, fmt, 4)
+    _check(orc, x, counts, q, sc, fmt)
