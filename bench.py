@@ -474,6 +474,48 @@ class E2EPipeline:
         comp.wait_stream(self.s_in)
         comp.wait_stream(self.s_out)
 
+    def link_rates(self, reps=3):
+        """Copy-engine rates of the host link in GB/s, measured on the
+        largest group's buffers: host->device alone, device->host alone, and
+        both directions at once (one copy each on the two copy streams).
+        The step's transfers take at least max(H2D bytes / h2d, D2H bytes /
+        d2h)."""
+        torch = self.torch
+        g = max(self.groups, key=lambda g: g["h_out"].numel())
+        comp = torch.cuda.current_stream()
+
+        def timed(fn):
+            fn()
+            torch.cuda.synchronize()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for _ in range(reps):
+                fn()
+            t1.record()
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1) / reps * 1e-3
+
+        def h2d():
+            g["d_in"].copy_(g["h_in"], non_blocking=True)
+
+        def d2h():
+            g["h_out"].copy_(g["d_out"], non_blocking=True)
+
+        def both():
+            self.s_in.wait_stream(comp)
+            self.s_out.wait_stream(comp)
+            with torch.cuda.stream(self.s_in):
+                h2d()
+            with torch.cuda.stream(self.s_out):
+                d2h()
+            comp.wait_stream(self.s_in)
+            comp.wait_stream(self.s_out)
+
+        b_in, b_out = g["h_in"].numel() * 2, g["h_out"].numel() * 2
+        return {"h2d_GBps": round(b_in / timed(h2d) / 1e9, 1),
+                "d2h_GBps": round(b_out / timed(d2h) / 1e9, 1),
+                "both_GBps": round((b_in + b_out) / timed(both) / 1e9, 1)}
+
 
 def timed_launches(bfq, torch, shapes, reps):
     """Per-launch durations (ms) of quant and GEMM for every shape, measured
@@ -1087,6 +1129,9 @@ def run_gpu(args, rank, world, local_rank):
     e_stop.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_stop), dist, dev)
+    link = pipe.link_rates()
+    link["transfer_bound_ms_per_step"] = round(1e3 * max(
+        h2d / (link["h2d_GBps"] * 1e9), d2h / (link["d2h_GBps"] * 1e9)), 3)
 
     if rank != 0:
         return 0
@@ -1118,7 +1163,8 @@ def run_gpu(args, rank, world, local_rank):
                 "how": "public C-ABI calls per shape; pinned host buffers, one H2D and one "
                        "D2H per (n,k) group of shapes; H2D, compute and D2H on three streams "
                        "ordered by events (transfers of one group overlap its neighbours' "
-                       "compute)"},
+                       "compute)",
+                "host_link": link},
         "gpu_launches": 2 * n_shapes * args.steps,
         "roofline": {"bound": "tensor", "achieved": round(achieved_tflops, 1),
                      "peak": fp8_peak, "unit": "TFLOP/s",
