@@ -236,3 +236,22 @@ def test_gemm_parity_persistent_many_tiles(cuda_lib, orc, fmt, M, N, K):
     got = out.float().cpu().numpy()
     assert_gemm_close(got[rows], ref, an, wn, f"persistent {M}x{N}x{K} fmt{fmt}")
     assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("fmt", [0, 2])
+@pytest.mark.parametrize("M,N,K", [(1280, 4096, 512), (2560, 2048, 1024), (2000, 2560, 256)])
+def test_gemm_persistent_partial_last_round(cuda_lib, orc, fmt, M, N, K):
+    """160 output tiles on a 152-SM part: the persistent schedule's second
+    round holds 8 tiles, the last row tiles of the last column tile (the
+    2000-row case ends in a ragged row tile).  Every element against the
+    oracle."""
+    bfq = cuda_lib
+    aq, sa, wq, sw = _oracle_problem(orc, M, N, K, fmt, seed=M + N + K + fmt)
+    d = _to_dev(aq, sa, wq, sw, fmt)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bfq.gemm(d[0], d[1], fmt, d[2], d[3], out=out)
+    torch.cuda.synchronize()
+    ref = orc.gemm(aq, sa, fmt, wq, sw)
+    an, wn = _norms(orc, aq, sa, wq, sw, fmt)
+    assert_gemm_close(out.float().cpu().numpy(), ref, an, wn, f"gemm {M}x{N}x{K} fmt{fmt}")
+    assert bfq.bfq_poll_device_status() == 0
