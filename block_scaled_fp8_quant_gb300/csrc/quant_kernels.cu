@@ -448,12 +448,16 @@ bfq_status launch_silu_mul_quant(const DeviceInfo& dev, dim3 grid, cudaStream_t 
   const int64_t E = grid.y;
   const int64_t n_x = E * T * 2 * (int64_t)I;
   const int64_t n_s = E * scale_cols(I, FMT) * scale_ld;
+  // Programmatic launch only when the whole grid (padded row pairs included)
+  // fits in one wave: a multi-wave grid launched early held SM slots while
+  // the GEMM before it ran (2 % of the MoE slice).
+  const int64_t blocks = (int64_t)grid.x * grid.y;
   if (tab)
-    return launch_status(launch_kernel(one_wave(silu_mul_quant_kernel<FMT, true>, dev, grid.x),
+    return launch_status(launch_kernel(one_wave(silu_mul_quant_kernel<FMT, true>, dev, blocks),
                                        silu_mul_quant_kernel<FMT, true>, grid,
                                        dim3(kQuantWarps * 32), 0, s, 1, x, T, I, counts, q,
                                        scales, scale_ld, tab, status, n_x, n_s));
-  return launch_status(launch_kernel(one_wave(silu_mul_quant_kernel<FMT, false>, dev, grid.x),
+  return launch_status(launch_kernel(one_wave(silu_mul_quant_kernel<FMT, false>, dev, blocks),
                                      silu_mul_quant_kernel<FMT, false>, grid,
                                      dim3(kQuantWarps * 32), 0, s, 1, x, T, I, counts, q, scales,
                                      scale_ld, tab, status, n_x, n_s));
