@@ -517,9 +517,11 @@ extern "C" bfq_status bfq_weight_block_quant(const void* w, int64_t batch, int64
   int* status = device_status_ptr();
   if (!status) return BFQ_ERR_CUDA;
   const int64_t n_w = batch * N * K, n_s = batch * NB * KB;  // debug bounds-check extents
+  // weight preparation keeps plain stream order (a multi-wave grid; nothing
+  // on the inference path waits on it)
   if (fmt == BFQ_SCALE_F32)
-    return launch_status(launch_pdl(weight_quant_kernel<false>, grid, dim3(256), 0, s, 1, wb, N,
-                                    K, wqb, sw, status, n_w, n_s));
-  return launch_status(launch_pdl(weight_quant_kernel<true>, grid, dim3(256), 0, s, 1, wb, N, K,
-                                  wqb, sw, status, n_w, n_s));
+    return launch_status(launch_kernel(false, weight_quant_kernel<false>, grid, dim3(256), 0, s,
+                                       1, wb, N, K, wqb, sw, status, n_w, n_s));
+  return launch_status(launch_kernel(false, weight_quant_kernel<true>, grid, dim3(256), 0, s, 1,
+                                     wb, N, K, wqb, sw, status, n_w, n_s));
 }

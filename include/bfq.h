@@ -26,8 +26,9 @@
  *    previous one in the stream is finishing, but it waits for that kernel's
  *    completion (and memory visibility) before it reads or writes any global
  *    memory, so stream order semantics are unchanged.  (Multi-wave quant
- *    grids keep plain stream order: launched early they slowed a sequence of
- *    GEMMs.)  Launches can be captured in CUDA graphs.
+ *    and silu-mul-quant grids keep plain stream order: launched early they
+ *    slowed the GEMMs around them.  So does bfq_weight_block_quant.)
+ *    Launches can be captured in CUDA graphs.
  *  - Arguments are validated on the host before anything is launched; an
  *    invalid call launches nothing and returns a non-zero bfq_status.  There
  *    is no CPU fallback and no alternative backend.
