@@ -323,7 +323,8 @@ namespace {
 // blocks resident at once).  Only such grids are launched with programmatic
 // dependent launch: a multi-wave quant grid launched early slowed the
 // 36-shape sweep step by ~1.5-3 % (measured with the launch mode split by
-// kernel), while a one-wave grid after a GEMM gains its set-up overlap.
+// kernel), a multi-wave silu-mul-quant grid the MoE slice by 2 %, while a
+// one-wave grid after a GEMM gains its set-up overlap.
 template <typename K>
 bool one_wave(K kernel, const DeviceInfo& dev, int64_t blocks) {
   static std::map<std::pair<const void*, int>, int> per_sm;
@@ -448,9 +449,8 @@ bfq_status launch_silu_mul_quant(const DeviceInfo& dev, dim3 grid, cudaStream_t 
   const int64_t E = grid.y;
   const int64_t n_x = E * T * 2 * (int64_t)I;
   const int64_t n_s = E * scale_cols(I, FMT) * scale_ld;
-  // Programmatic launch only when the whole grid (padded row pairs included)
-  // fits in one wave: a multi-wave grid launched early held SM slots while
-  // the GEMM before it ran (2 % of the MoE slice).
+  // programmatic launch only when the whole grid (padded row pairs included)
+  // fits in one wave
   const int64_t blocks = (int64_t)grid.x * grid.y;
   if (tab)
     return launch_status(launch_kernel(one_wave(silu_mul_quant_kernel<FMT, true>, dev, blocks),
